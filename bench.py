@@ -1,0 +1,321 @@
+"""Benchmark of the gated delta rule layer on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill (pre-pass, block kernel, varlen/tail handling) of one 4096-token
+    sequence, Hk=16, Hv=32, dk=dv=128, bf16 I/O, fp32 state, chunk 64, zero
+    initial state;
+  * one decode step of 128 sequences with the same heads (fp32 state
+    ~N(0, 0.02), in place).
+
+`value` is the prefill throughput (Mtok/s); the decode step's time is under
+"decode" (us/step). Both are timed with CUDA events on the stream the
+kernels are launched on, L2 flushed (a 256 MiB write) before each timed
+launch. `--impl reference` times the fp64 CPU oracle on the same workload
+(a bounded sample) instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+import torch.distributed as dist
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_PREFILL, HK, HV, DK, DV, CHUNK = 4096, 16, 32, 128, 128, 64
+N_DECODE = 128
+METRIC = "Gated-DeltaNet prefill Mtok/s & decode µs/step (1 GB300); % of roofline"
+WORKLOAD = ("prefill B=1 T=4096 Hk=16 Hv=32 dk=dv=128 chunk=64 bf16, zero state; "
+            "then decode step N=128 same heads, fp32 state")
+
+# algorithmic bytes/flops (per token / per sequence)
+IO_BYTES_PER_TOKEN = (HK * DK * 2 * 2) + (HV * DV * 2) * 2 + HV * 2 * 2  # q,k + v,out + g,b
+STATE_BYTES = HV * DV * DK * 4
+PREFILL_BYTES = T_PREFILL * IO_BYTES_PER_TOKEN + STATE_BYTES  # state written once (zero state in)
+PREFILL_FLOPS_PER_TOKEN = HV * (5 * 2 * CHUNK * DK + 3 * 2 * DK * DV)  # chunk GEMMs (dk == dv)
+DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + IO_BYTES_PER_TOKEN
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_inputs(dev):
+    from gated_deltanet_linear_delta_gb300 import inputs
+    pb = inputs.prefill_4k(seed=0)
+    q, k, v, g, b, st = inputs.make_decode_inputs(N_DECODE, seed=0)
+    return pb, (q[0], k[0], v[0], g[0], b[0], st)
+
+
+def run_ours(args, rank, world):
+    import gated_deltanet_linear_delta_gb300 as gdn
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    pb, dec = make_inputs(dev)
+    d = pb.to(dev)
+    out = torch.empty(T_PREFILL, HV, DV, dtype=torch.bfloat16, device=dev)
+    st_out = torch.empty(1, HV, DV, DK, device=dev)
+    qd, kd, vd, gd, bd = (x.to(dev) for x in dec[:5])
+    state0 = dec[5].to(dev)
+    dstate = state0.clone()
+    dout = torch.empty(N_DECODE, HV, DV, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        gdn.gdn_prefill(d.q, d.k, d.v, d.g, d.b, None, st_out, out, None, B=1, chunk=CHUNK, stream=stream)
+
+    def decode():
+        gdn.gdn_decode_step(qd, kd, vd, gd, bd, dstate, dout, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        prefill()
+        flush.fill_(2.0)
+        decode()
+    torch.cuda.synchronize()
+    if gdn.gdn_get_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device status reports an inconsistency")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(dev.index) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(1.0)
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            flush.fill_(2.0)
+            ev[i][2].record(stream)
+            decode()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    pre_mean, dec_mean = sum(pre_ms) / len(pre_ms), sum(dec_ms) / len(dec_ms)
+    step_ms = pre_mean + dec_mean
+    if world > 1:
+        t = torch.tensor([pre_mean, dec_mean, step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        pre_mean, dec_mean, step_ms = (float(x) for x in t)
+
+    # decode batch sweep (same kernel, smaller batches), L2 flushed before each launch
+    sweep = {}
+    for n in (1, 8, 32, 128):
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(3.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gdn.gdn_decode_step(qd[:n], kd[:n], vd[:n], gd[:n], bd[:n], dstate[:n], dout[:n], stream=stream)
+            e1.record(stream)
+            if i >= args.warmup:
+                times.append((e0, e1))
+        torch.cuda.synchronize()
+        us = 1e3 * sum(a.elapsed_time(b) for a, b in times) / len(times)
+        sweep[str(n)] = round(us, 3)
+
+    e2e = measure_e2e(args, gdn, pb, dec, dev, stream)
+    hbm, bf16, src = peaks()
+    pre_s = pre_mean / 1e3
+    achieved_gbs = PREFILL_BYTES / pre_s / 1e9
+    achieved_tfs = PREFILL_FLOPS_PER_TOKEN * T_PREFILL / pre_s / 1e12
+    roof_time = max(PREFILL_BYTES / (hbm * 1e9), PREFILL_FLOPS_PER_TOKEN * T_PREFILL / (bf16 * 1e12))
+    dec_bytes = N_DECODE * DECODE_BYTES_PER_SEQ
+    dec_gbs = dec_bytes / (dec_mean / 1e3) / 1e9
+    path = gdn.gdn_prefill_path(1, T_PREFILL, HK, HV, DK, DV, CHUNK, gdn.GDN_BF16)
+    clocks = clk.summary()
+    value = world * T_PREFILL / pre_s / 1e6
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "Mtok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, g=-softplus(N(0,1)), beta logits N(0,1))",
+        "config": {"workload": WORKLOAD, "prefill_tokens": T_PREFILL, "decode_batch": N_DECODE,
+                   "Hk": HK, "Hv": HV, "dk": DK, "dv": DV, "chunk": CHUNK,
+                   "l2": "flushed: 256 MiB write before each timed launch",
+                   "prefill_kernel": {1: "tcgen05 block kernel", 0: "CUDA-core block kernel"}.get(path, path),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "prefill": {"ms": round(pre_mean, 5), "Mtok_s": round(T_PREFILL / pre_s / 1e6, 3),
+                    "GB_s": round(achieved_gbs, 1), "TFLOP_s": round(achieved_tfs, 2),
+                    "roofline_ms": round(roof_time * 1e3, 5), "frac_of_roofline": round(roof_time / pre_s, 4)},
+        "decode": {"value": round(dec_mean * 1e3, 3), "unit": "us/step", "batch": N_DECODE,
+                   "higher_is_better": False, "GB_s": round(dec_gbs, 1),
+                   "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                                "frac": round(dec_gbs / hbm, 4), "traffic": None,
+                                "peak_source": src},
+                   "sweep_us": sweep},
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved_gbs / hbm, 4), "traffic": None, "peak_source": src,
+                     "kernel": "prefill"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    return line
+
+
+def measure_e2e(args, gdn, pb, dec, dev, stream):
+    """Same prefill through the public API with pinned host buffers; copies inside the timed region."""
+    host = {n: getattr(pb, n).pin_memory() for n in ("q", "k", "v", "g", "b")}
+    dbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out = torch.empty(T_PREFILL, HV, DV, dtype=torch.bfloat16, device=dev)
+    st = torch.empty(1, HV, DV, DK, device=dev)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_st = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_out.numel() * h_out.element_size() + h_st.numel() * h_st.element_size()
+    times = []
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for n in host:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        gdn.gdn_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["b"], None, st, out, None, B=1,
+                        chunk=CHUNK, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_st.copy_(st, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    mean = sum(times) / len(times)
+    return {"value": round(T_PREFILL / mean / 1e6, 3), "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(mean * 1e3, 4)}
+
+
+def cpu_baseline_sample(threads=None, tokens=T_PREFILL, steps=1, warmup=0):
+    """The fp64 oracle (token scan, as it stands), all 32 heads, on the first `tokens` tokens of
+    the prefill prompt, one thread per (sequence, head) unit up to `threads`."""
+    import oracle
+    from gated_deltanet_linear_delta_gb300 import inputs
+    pb = inputs.prefill_4k(seed=0)
+    threads = threads or (os.cpu_count() or 1)
+    sl = slice(0, tokens)
+    args = [x[sl].double().numpy() for x in (pb.q, pb.k, pb.v, pb.g, pb.b)]
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        oracle.gdn_sequential(*args, None, None, B=1, threads=threads)
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    dt = sum(times) / len(times)
+    return {"value": round(tokens / dt / 1e6, 6), "unit": "Mtok/s", "cores": min(threads, HV), "kind": "oracle",
+            "sample": f"{tokens} tokens of the 4096-token prompt, all 32 value heads, fp64 token scan",
+            "seconds_per_pass": round(dt, 3)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        # the oracle on the host cores; rank 0 only
+        if rank != 0:
+            return
+        base = cpu_baseline_sample(steps=args.steps, warmup=args.warmup)
+        line = {"metric": METRIC, "value": base["value"], "unit": "Mtok/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "ms_per_step": round(1e3 * base["seconds_per_pass"], 3),
+                "config": {"workload": WORKLOAD, "reference": "fp64 CPU oracle (token scan), bounded sample"},
+                "cpu_baseline": base,
+                "e2e": {"value": base["value"], "unit": "Mtok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline_sample()
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

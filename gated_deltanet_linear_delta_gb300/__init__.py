@@ -1,0 +1,166 @@
+"""GB300 (sm_103a) gated delta rule layer: thin Python binding of the C ABI.
+
+Every function here only marshals arguments (shapes, dtypes, device pointers,
+the current CUDA stream) and calls the entry point of the same name in
+``libgdn_gb300.so`` (declared in ``include/gdn.h``). All arithmetic runs in
+the library's CUDA kernels. There is no CPU fallback: if the library is not
+built, every call raises.
+
+Tensors are torch CUDA tensors, contiguous, in the layouts of ``gdn.h``:
+q, k [Ttot, Hk, dk]; v, out [Ttot, Hv, dv]; g, b [Ttot, Hv] (bf16 or fp32,
+all the same dtype); states [B, Hv, dv, dk] fp32; cu_seqlens int32 [B+1].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = ["GDNError", "gdn_prefill", "gdn_decode_step", "gdn_prepass", "gdn_prefill_path",
+           "gdn_get_device_status", "gdn_status_string", "library", "library_path",
+           "GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
+           "GDN_ERR_DEVICE_CHECK", "GDN_BF16", "GDN_F32"]
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_CHECK = 0, -1, -2, -3, -4
+GDN_BF16, GDN_F32 = 0, 1
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where} returned {gdn_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def library() -> ctypes.CDLL:
+    """Load libgdn_gb300.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"the CUDA library {path} is not built; run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            lib.gdn_prefill.argtypes = [_P] * 9 + [_I] * 8 + [_P]
+            lib.gdn_prefill.restype = _I
+            lib.gdn_decode_step.argtypes = [_P] * 7 + [_I] * 6 + [_P]
+            lib.gdn_decode_step.restype = _I
+            lib.gdn_prepass.argtypes = [_P] * 5 + [_I] * 7 + [_P] * 4 + [_P]
+            lib.gdn_prepass.restype = _I
+            lib.gdn_prefill_path.argtypes = [_I] * 8
+            lib.gdn_prefill_path.restype = _I
+            lib.gdn_get_device_status.argtypes = [_P]
+            lib.gdn_get_device_status.restype = _I
+            lib.gdn_status_string.argtypes = [_I]
+            lib.gdn_status_string.restype = ctypes.c_char_p
+            _lib = lib
+        return _lib
+
+
+def gdn_status_string(status: int) -> str:
+    return library().gdn_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != GDN_OK:
+        raise GDNError(rc, where)
+
+
+def gdn_prefill(q, k, v, g, b, state_in, state_out, out, cu_seqlens=None, B=None, T=None, chunk=64,
+                stream=None) -> None:
+    """Chunked prefill over packed sequences; writes `out` and `state_out` (may alias state_in)."""
+    Ttot, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        B, T = cu_seqlens.numel() - 1, Ttot
+    else:
+        B = 1 if B is None else B
+        T = Ttot // B if T is None else T
+    dt = _dtype_code(q)
+    for t in (k, v, g, b, out):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v, g, b and out must share one dtype")
+    for t in (state_in, state_out):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("states are fp32")
+    rc = library().gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_in),
+                               _ptr(state_out), _ptr(out), _ptr(cu_seqlens), B, T, Hk, Hv, dk, dv,
+                               chunk, dt, _stream(stream))
+    _check(rc, "gdn_prefill")
+
+
+def gdn_decode_step(q, k, v, g, b, state, out, stream=None) -> None:
+    """One decode step for N sequences; updates `state` in place and writes `out`."""
+    N, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    dt = _dtype_code(q)
+    if state.dtype != torch.float32:
+        raise TypeError("the state is fp32")
+    rc = library().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state), _ptr(out),
+                                   N, Hk, Hv, dk, dv, dt, _stream(stream))
+    _check(rc, "gdn_decode_step")
+
+
+def gdn_prepass(q, k, g, b, rq, rk, beta, gcum, cu_seqlens=None, B=None, T=None, chunk=64,
+                stream=None) -> None:
+    """Per-token inverse norms, beta and in-block cumulative gate (fp32 outputs)."""
+    Ttot, Hk, dk = q.shape
+    Hv = g.shape[1]
+    if cu_seqlens is not None:
+        B, T = cu_seqlens.numel() - 1, Ttot
+    else:
+        B = 1 if B is None else B
+        T = Ttot // B if T is None else T
+    rc = library().gdn_prepass(_ptr(q), _ptr(k), _ptr(g), _ptr(b), _ptr(cu_seqlens), B, T, Hk, Hv, dk,
+                               chunk, _dtype_code(q), _ptr(rq), _ptr(rk), _ptr(beta), _ptr(gcum),
+                               _stream(stream))
+    _check(rc, "gdn_prepass")
+
+
+def gdn_prefill_path(B, T, Hk, Hv, dk, dv, chunk, dtype) -> int:
+    """1 = tensor-core kernel, 0 = CUDA-core kernel, <0 = the status gdn_prefill would return."""
+    if isinstance(dtype, torch.dtype):
+        dtype = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    return library().gdn_prefill_path(B, T, Hk, Hv, dk, dv, chunk, int(dtype))
+
+
+def gdn_get_device_status(stream=None) -> int:
+    """Synchronise the stream, return and clear the device status word."""
+    return library().gdn_get_device_status(_stream(stream))

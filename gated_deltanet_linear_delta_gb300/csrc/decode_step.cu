@@ -1,0 +1,133 @@
+// decode_step.cu -- one recurrent step of the gated delta rule for N sequences.
+//
+// Decoding is bound by the bytes moved per token ("Optimiser l'inference sur
+// appareil pour Apple Silicon", section "Decodage : minimiser les octets
+// deplaces par token"): per (sequence, value head) the fp32 state S
+// (dv x dk) is read once and written once, in place. Everything else -- the
+// L2 normalisation of q and k, alpha = exp(g), beta = sigmoid(b), the delta
+// update and the read-out -- is fused into the same pass (section "Reduire le
+// trafic intermediaire et d'etat": the recurrent update is fused with its
+// normalisation). Adjacent lanes read adjacent 16-byte pieces of a state row
+// (section "Fusionner les lectures du cache d'attention": neighbouring threads
+// should ask for neighbouring bytes).
+//
+// Per row i of S, with kh, qh the normalised key/query of the shared key head:
+//     e_i = alpha (S kh)_i,   u_i = beta (v_i - e_i)
+//     S_i <- alpha S_i + u_i kh^T
+//     o_i = (S_new qh)_i = alpha (S qh)_i + u_i (kh . qh)
+// so both dot products S_i.kh and S_i.qh come from the single read of S_i and
+// are reduced together across the lanes that hold the row.
+//
+// Work mapping: a row of dk fp32 is held by LPR = dk/4 lanes, one float4 each;
+// a warp covers RPW = 32/LPR rows per pass and R passes, all R loads issued
+// before any arithmetic so that 16*R bytes per thread are in flight. All rows
+// of one warp belong to one (sequence, head), so the norms are computed once
+// per warp.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+constexpr int kDecodeRows = 4;  // passes (rows per lane group) per warp
+
+template <int DK, int DV, typename TIn>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
+                   const TIn *__restrict__ g, const TIn *__restrict__ b, float *__restrict__ state,
+                   TIn *__restrict__ out, int N, int Hk, int Hv) {
+    constexpr int LPR = DK / 4;    // lanes per row
+    constexpr int RPW = 32 / LPR;  // rows per warp pass
+    constexpr int R = kDecodeRows;
+    constexpr int ROWS_PER_WARP = RPW * R;
+    static_assert(DV % ROWS_PER_WARP == 0, "a warp must stay within one head");
+
+    const int lane = threadIdx.x & 31;
+    const long warp = (long)blockIdx.x * (kDecodeThreads / 32) + (threadIdx.x >> 5);
+    const long row0 = warp * ROWS_PER_WARP;
+    const long total_rows = (long)N * Hv * DV;
+    if (row0 >= total_rows) return;
+
+    const long nh = row0 / DV;  // (sequence, value head) index = n*Hv + h
+    const int i0 = (int)(row0 % DV);
+    const int h = (int)(nh % Hv);
+    const long n = nh / Hv;
+    const int hk = h / (Hv / Hk);
+    const int grp = lane / LPR;  // row within a pass
+    const int c = lane % LPR;    // float4 column
+
+    // issue the state loads first: they are the bytes that matter
+    float *srow[R];
+    float4 s[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int i = i0 + r * RPW + grp;
+        srow[r] = state + (nh * DV + i) * (long)DK + 4 * c;
+        s[r] = __ldcs(reinterpret_cast<const float4 *>(srow[r]));
+    }
+    const long kq_off = (n * Hk + hk) * (long)DK + 4 * c;
+    const float4 k4 = load4(k + kq_off);
+    const float4 q4 = load4(q + kq_off);
+    float vi[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) vi[r] = to_f32(v[nh * DV + i0 + r * RPW + grp]);
+    const float alpha = expf(to_f32(g[nh]));
+    const float beta = sigmoidf_(to_f32(b[nh]));
+
+    // L2 norms of the shared key head (every lane group holds a full copy)
+    const float ssk = group_sum<LPR>(dot4(k4, k4));
+    const float ssq = group_sum<LPR>(dot4(q4, q4));
+    const float skq = group_sum<LPR>(dot4(k4, q4));
+    const float rk = rsqrtf(ssk + kNormEps), rq = rsqrtf(ssq + kNormEps);
+    const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+    const float4 qh = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+    const float kq = skq * rk * rq;
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float sk = group_sum<LPR>(dot4(s[r], kh));
+        const float sq = group_sum<LPR>(dot4(s[r], qh));
+        const float u = beta * (vi[r] - alpha * sk);
+        float4 o4;
+        o4.x = alpha * s[r].x + u * kh.x;
+        o4.y = alpha * s[r].y + u * kh.y;
+        o4.z = alpha * s[r].z + u * kh.z;
+        o4.w = alpha * s[r].w + u * kh.w;
+        __stcs(reinterpret_cast<float4 *>(srow[r]), o4);
+        if (c == 0) out[nh * DV + i0 + r * RPW + grp] = from_f32<TIn>(alpha * sq + u * kq);
+    }
+}
+
+template <int DK, int DV, typename TIn>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
+    constexpr int ROWS_PER_WARP = (32 / (DK / 4)) * kDecodeRows;
+    const long rows = (long)a.N * a.Hv * DV;
+    const long warps = (rows + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
+    const long blocks = (warps + kDecodeThreads / 32 - 1) / (kDecodeThreads / 32);
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    decode_step_kernel<DK, DV, TIn><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(
+        (const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, (const TIn *)a.g, (const TIn *)a.b,
+        a.state, (TIn *)a.out, a.N, a.Hk, a.Hv);
+    return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t dispatch_dims(const DecodeArgs &a, cudaStream_t s) {
+#define GDN_DECODE_CASE(DKV, DVV) \
+    if (a.dk == DKV && a.dv == DVV) return launch_t<DKV, DVV, TIn>(a, s);
+    GDN_DECODE_CASE(32, 32) GDN_DECODE_CASE(32, 64) GDN_DECODE_CASE(32, 128)
+    GDN_DECODE_CASE(64, 32) GDN_DECODE_CASE(64, 64) GDN_DECODE_CASE(64, 128)
+    GDN_DECODE_CASE(128, 32) GDN_DECODE_CASE(128, 64) GDN_DECODE_CASE(128, 128)
+#undef GDN_DECODE_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
+    if (a.N == 0) return cudaSuccess;
+    return a.dtype == GDN_BF16 ? dispatch_dims<__nv_bfloat16>(a, s) : dispatch_dims<float>(a, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,158 @@
+// gdn_api.cu -- the exported C ABI: argument checks, the device status word,
+// and dispatch to the kernels. Every check runs before any device work is
+// queued; a failed check returns its gdn_status and touches nothing.
+#include <stdint.h>
+
+#include <cuda_runtime.h>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+// Device-side consistency flag, one per device (a __device__ variable has one
+// instance per device context). Kernels set it with atomicExch; the host reads
+// and clears it in gdn_get_device_status.
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices] = {nullptr};
+
+int *status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+bool chunk_ok(int c) { return c == 16 || c == 32 || c == 64; }
+
+int common_checks(int Hk, int Hv, int dk, int dv, int dtype) {
+    if (Hk <= 0 || Hv <= 0 || Hv % Hk != 0 || Hv > 65535) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+    if (!dim_ok(dk) || !dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+int prefill_checks(const void *q, const void *k, const void *v, const void *g, const void *b,
+                   const float *state_in, const float *state_out, const void *out,
+                   const int32_t *cu, int B, int T, int Hk, int Hv, int dk, int dv, int chunk,
+                   int dtype) {
+    if (B < 0 || T < 0 || B > 65535) return GDN_ERR_INVALID_ARG;
+    int rc = common_checks(Hk, Hv, dk, dv, dtype);
+    if (rc != GDN_OK) return rc;
+    if (!chunk_ok(chunk)) return GDN_ERR_UNSUPPORTED;
+    if (B == 0) return GDN_OK;
+    const long long Ttot = cu ? (long long)T : (long long)B * T;
+    if (Ttot > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+    if (!state_out) return GDN_ERR_INVALID_ARG;
+    if (Ttot > 0 && (!q || !k || !v || !g || !b || !out)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, b, state_in, state_out, out, cu};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK";
+    }
+    return "GDN_UNKNOWN_STATUS";
+}
+
+int gdn_prefill_path(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype) {
+    // a dummy aligned address stands in for every pointer: only sizes are checked
+    static __align__(16) char dummy[16];
+    const void *p = dummy;
+    int rc = prefill_checks(p, p, p, p, p, nullptr, (const float *)p, p, nullptr, B, T, Hk, Hv, dk,
+                            dv, chunk, dtype);
+    if (rc != GDN_OK) return rc;
+    gdn::PrefillArgs a{};
+    a.B = B; a.T = T; a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv; a.chunk = chunk; a.dtype = dtype;
+    return gdn::prefill_tc_supported(a) ? 1 : 0;
+}
+
+int gdn_prefill(const void *q, const void *k, const void *v, const void *g, const void *b,
+                const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
+                int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype, void *stream) {
+    int rc = prefill_checks(q, k, v, g, b, state_in, state_out, out, cu_seqlens, B, T, Hk, Hv, dk,
+                            dv, chunk, dtype);
+    if (rc != GDN_OK) return rc;
+    if (B == 0) return GDN_OK;
+    int *status = status_ptr();
+    if (!status) return GDN_ERR_CUDA;
+    gdn::PrefillArgs a{q, k, v, g, b, state_in, state_out, out, cu_seqlens,
+                       B, T, Hk, Hv, dk, dv, chunk, dtype, status};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = gdn::prefill_tc_supported(a) ? gdn::launch_prefill_tc(a, s)
+                                                       : gdn::launch_prefill_simt(a, s);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *b,
+                    float *state, void *out, int N, int Hk, int Hv, int dk, int dv, int dtype,
+                    void *stream) {
+    if (N < 0) return GDN_ERR_INVALID_ARG;
+    int rc = common_checks(Hk, Hv, dk, dv, dtype);
+    if (rc != GDN_OK) return rc;
+    if (N == 0) return GDN_OK;
+    if ((long long)N * Hv * dv * dk > (1LL << 40)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, b, state, out};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    gdn::DecodeArgs a{q, k, v, g, b, state, out, N, Hk, Hv, dk, dv, dtype};
+    return gdn::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
+                                                                                   : GDN_ERR_CUDA;
+}
+
+int gdn_prepass(const void *q, const void *k, const void *g, const void *b,
+                const int32_t *cu_seqlens, int B, int T, int Hk, int Hv, int dk, int chunk,
+                int dtype, float *rq, float *rk, float *beta, float *gcum, void *stream) {
+    if (B < 0 || T < 0 || B > 65535) return GDN_ERR_INVALID_ARG;
+    int rc = common_checks(Hk, Hv, dk, 32, dtype);
+    if (rc != GDN_OK) return rc;
+    if (!chunk_ok(chunk)) return GDN_ERR_UNSUPPORTED;
+    const long long Ttot = cu_seqlens ? (long long)T : (long long)B * T;
+    if (Ttot > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+    if (B == 0 || Ttot == 0) return GDN_OK;
+    const void *ptrs[] = {q, k, g, b, rq, rk, beta, gcum};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned16(cu_seqlens)) return GDN_ERR_INVALID_ARG;
+    int *status = status_ptr();
+    if (!status) return GDN_ERR_CUDA;
+    gdn::PrepassArgs a{q, k, g, b, cu_seqlens, B, T, Hk, Hv, dk, chunk, dtype, rq, rk, beta, gcum,
+                       status};
+    return gdn::launch_prepass(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
+                                                                                     : GDN_ERR_CUDA;
+}
+
+int gdn_get_device_status(void *stream) {
+    int *status = status_ptr();
+    if (!status) return GDN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+    int host = 0;
+    if (cudaMemcpy(&host, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return host == 0 ? GDN_OK : GDN_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

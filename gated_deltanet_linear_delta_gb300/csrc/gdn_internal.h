@@ -1,0 +1,40 @@
+// gdn_internal.h -- launchers behind the C ABI (host side, not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct PrefillArgs {
+    const void *q, *k, *v, *g, *b;
+    const float *state_in;
+    float *state_out;
+    void *out;
+    const int32_t *cu_seqlens;
+    int B, T, Hk, Hv, dk, dv, chunk, dtype;
+    int *status;  // device status word
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v, *g, *b;
+    float *state;
+    void *out;
+    int N, Hk, Hv, dk, dv, dtype;
+};
+
+struct PrepassArgs {
+    const void *q, *k, *g, *b;
+    const int32_t *cu_seqlens;
+    int B, T, Hk, Hv, dk, chunk, dtype;
+    float *rq, *rk, *beta, *gcum;
+    int *status;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_prepass(const PrepassArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
+bool prefill_tc_supported(const PrefillArgs &a);
+
+}  // namespace gdn

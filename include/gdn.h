@@ -1,0 +1,158 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta rule layer.
+ *
+ * The layer keeps, per sequence and value head, a fixed-size matrix state
+ * S in R^{dv x dk}. A learned gate decides how much of the old state to keep
+ * and a delta update writes the current token into it; every token depends on
+ * the state left by the previous one ("Optimiser l'inference sur appareil
+ * pour Apple Silicon", section "Qwen cree trois formes de charges de
+ * travail"). With qh = q/sqrt(|q|^2+1e-6), kh likewise, alpha = exp(g),
+ * beta = sigmoid(b), one token does
+ *
+ *     S <- alpha S (I - beta kh kh^T) + beta v kh^T,      o = S qh
+ *
+ * (the read-out uses the updated state). State and gate arithmetic is fp32
+ * because rounding accumulates over sequential updates, while q/k/v stay in
+ * bf16 (same page, section "Maintenir l'etat recurrent sur la puce").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array arguments are DEVICE pointers owned by the caller; the library
+ *    never frees or keeps them. Every pointer must be 16-byte aligned.
+ *  - Packed token layouts, row-major:
+ *        q, k   [Ttot][Hk][dk]        v, out [Ttot][Hv][dv]
+ *        g, b   [Ttot][Hv]            (g: log-decay; b: beta logit)
+ *        state  [B][Hv][dv][dk] fp32  (row i of S is contiguous)
+ *  - Value head h reads key head h / (Hv/Hk) (consecutive value heads share
+ *    a key head); Hv must be a multiple of Hk.
+ *  - `dtype` (gdn_dtype) is the element type of q, k, v, g, b and out; the
+ *    state is always fp32.
+ *  - q and k are raw: the library L2-normalises them per head.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on it and never synchronise it, except
+ *    gdn_get_device_status.
+ *  - Argument errors are reported by the return value before any device work
+ *    is queued; nothing aborts or exits the process.
+ *  - Inconsistent device-side data that the host cannot see (cu_seqlens not
+ *    starting at 0, decreasing, or not ending at T) is reported through the
+ *    library's device status word; the affected sequences are skipped.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer */
+    GDN_ERR_UNSUPPORTED = -2,  /* valid but unsupported dk/dv/chunk/dtype    */
+    GDN_ERR_CUDA = -3,         /* a CUDA runtime/driver call failed          */
+    GDN_ERR_DEVICE_CHECK = -4  /* a kernel found inconsistent device data    */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
+
+/*
+ * gdn_prefill -- run the recurrence over whole prompts (chunked prefill).
+ *
+ * Evaluates the same function as the token scan by regrouping each run of
+ * `chunk` tokens into a block whose updates become matrix products ("Qwen cree
+ * trois formes de charges de travail": blocks expose matrix operations and
+ * token-level parallelism). Within a block of L tokens starting from state
+ * S0, with G_t the in-block cumulative log-gate:
+ *     A_ts = beta_t e^{G_t-G_s} kh_t.kh_s (s<t),   T = (I + A)^-1,
+ *     U    = T diag(beta) V - T diag(beta e^G) Kh S0^T,
+ *     O    = diag(e^G) Qh S0^T + P U,   P_ts = e^{G_t-G_s} qh_t.kh_s (s<=t),
+ *     S    = e^{G_L} S0 + U^T diag(e^{G_L-G_t}) Kh.
+ * The state enters from state_in and leaves in state_out, so a long prompt may
+ * be cut into fragments whose state is carried from one call to the next with
+ * an unchanged result ("Limiter la memoire temporaire grace au decoupage des
+ * prompts").
+ *
+ *   q, k, v, g, b : packed inputs (layouts above), Ttot tokens.
+ *   state_in      : [B][Hv][dv][dk] fp32 initial states, or NULL for zeros.
+ *   state_out     : [B][Hv][dv][dk] fp32 final states; may equal state_in
+ *                   (in-place update). A zero-length sequence copies its
+ *                   initial state through.
+ *   out           : [Ttot][Hv][dv] outputs, dtype `dtype`.
+ *   cu_seqlens    : device int32 [B+1] sequence offsets (0 = cu[0] <= ... <=
+ *                   cu[B] = T), or NULL: B sequences of T tokens each
+ *                   (Ttot = B*T).
+ *   B, T          : sequence count; tokens per sequence (cu_seqlens NULL) or
+ *                   total packed tokens (cu_seqlens given).
+ *   Hk, Hv, dk, dv: head counts and head dimensions; dk, dv in {32, 64, 128}.
+ *   chunk         : block length, one of 16, 32, 64.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
+ */
+GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void *g, const void *b,
+                const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
+                int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype, void *stream);
+
+/*
+ * gdn_decode_step -- one recurrent step for N independent sequences.
+ *
+ * Decoding is bound by the bytes moved per token ("Decodage : minimiser les
+ * octets deplaces par token"); this step reads each head's fp32 state once
+ * and writes it once, in place, fusing normalisation, gates, update and
+ * read-out in one launch (same page, section "Reduire le trafic
+ * intermediaire et d'etat": the recurrent update is fused with its
+ * normalisation so no intermediate goes through memory).
+ *
+ *   q, k  : [N][Hk][dk];  v : [N][Hv][dv];  g, b : [N][Hv]   (dtype `dtype`)
+ *   state : [N][Hv][dv][dk] fp32, updated in place.
+ *   out   : [N][Hv][dv] (dtype `dtype`), o = S_new qh.
+ *   N     : sequences (N = 0 is a no-op returning GDN_OK).
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
+ */
+GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *b,
+                    float *state, void *out, int N, int Hk, int Hv, int dk, int dv, int dtype,
+                    void *stream);
+
+/*
+ * gdn_prepass -- the per-token quantities of the block form, materialised.
+ *
+ * gdn_prefill computes these inside its kernels and never writes them; this
+ * entry point exposes the same computation for inspection and testing:
+ *   rq, rk : [Ttot][Hk] fp32, 1/sqrt(|q_t|^2 + 1e-6) and likewise for k;
+ *   beta   : [Ttot][Hv] fp32, sigmoid(b_t);
+ *   gcum   : [Ttot][Hv] fp32, sum of g over t's block up to and including t,
+ *            blocks starting at every sequence start and every `chunk` tokens.
+ * Other arguments as for gdn_prefill (dk in {32, 64, 128}).
+ */
+GDN_API int gdn_prepass(const void *q, const void *k, const void *g, const void *b,
+                const int32_t *cu_seqlens, int B, int T, int Hk, int Hv, int dk, int chunk,
+                int dtype, float *rq, float *rk, float *beta, float *gcum, void *stream);
+
+/*
+ * gdn_prefill_path -- which kernel gdn_prefill would launch for these sizes:
+ * 1 = tensor-core block kernel (tcgen05/TMEM/TMA), 0 = CUDA-core block kernel,
+ * negative = the gdn_status gdn_prefill would return. Host-only, no device work.
+ */
+GDN_API int gdn_prefill_path(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype);
+
+/*
+ * gdn_get_device_status -- synchronise `stream`, then return and clear the
+ * device status word: GDN_OK, or GDN_ERR_DEVICE_CHECK if a kernel found
+ * inconsistent device data since the last call; GDN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+GDN_API int gdn_get_device_status(void *stream);
+
+/* gdn_status_string -- static, human-readable name of a gdn_status value. */
+GDN_API const char *gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

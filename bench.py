@@ -67,13 +67,19 @@ class Clocks:
         self.file = None
 
     def __enter__(self):
+        self.t0 = time.time()
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
+            return self
+        # wait for the first sample so that the timed region is covered
+        deadline = time.time() + 5.0
+        while time.time() < deadline and os.path.getsize(self.file.name) == 0:
+            time.sleep(0.02)
         return self
 
     def __exit__(self, *a):
@@ -283,7 +289,7 @@ def cpu_baseline_sample(threads=None, tokens=T_PREFILL, steps=1, warmup=0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

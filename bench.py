@@ -44,6 +44,9 @@ STATE_BYTES = HV * DV * DK * 4
 PREFILL_BYTES = T_PREFILL * IO_BYTES_PER_TOKEN + STATE_BYTES  # state written once (zero state in)
 PREFILL_FLOPS_PER_TOKEN = HV * (5 * 2 * CHUNK * DK + 3 * 2 * DK * DV)  # chunk GEMMs (dk == dv)
 DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + IO_BYTES_PER_TOKEN
+# DRAM bytes per launch from the committed ncu captures (profiles/); None once a kernel
+# has changed since its capture.
+TRAFFIC = {"prefill": None, "decode": 480.2e6}
 
 
 def peaks():
@@ -223,11 +226,11 @@ def run_ours(args, rank, world):
         "decode": {"value": round(dec_mean * 1e3, 3), "unit": "us/step", "batch": N_DECODE,
                    "higher_is_better": False, "GB_s": round(dec_gbs, 1),
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
-                                "frac": round(dec_gbs / hbm, 4), "traffic": None,
+                                "frac": round(dec_gbs / hbm, 4), "traffic": TRAFFIC["decode"],
                                 "peak_source": src},
                    "sweep_us": sweep},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved_gbs / hbm, 4), "traffic": None, "peak_source": src,
+                     "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC["prefill"], "peak_source": src,
                      "kernel": "prefill"},
         "clocks": clocks,
         "e2e": e2e,

@@ -1,5 +1,5 @@
 // prefill_tc.cu -- block (chunk) form of the gated delta rule on the sm_103a
-// tensor cores: TMA tile loads, tcgen05.mma into tensor memory (TMEM), fp32
+// tensor cores: TMA tile loads, tcgen05.mma into tensor memory (TMEM), the fp32
 // state carried on chip across all blocks of a sequence.
 //
 // The pages describe two evaluation orders of the recurrence: a direct token
@@ -10,28 +10,39 @@
 // recurrent sur la puce"). This kernel is the block order for dk = dv = 128,
 // blocks of C = 64 tokens, bf16 I/O.
 //
-// Notation for one block of L <= 64 tokens of value head h, entering state S
-// (dv x dk, fp32), raw bf16 tiles K, Q (C x dk) and V (C x dv), per-token
-// rk, rq (inverse L2 norms), beta = sigmoid(b), G = in-block cumulative g,
+// Per block of L <= 64 tokens of value head h, entering state S (dv x dk, fp32),
+// with Kh, Qh the L2-normalised key/query rows, G the in-block cumulative log-gate,
 // e_t = exp(G_t), d_t = exp(G_{L-1} - G_t), gamma = exp(G_{L-1}):
-//   Gram:  [K; Q] K^T                      -> A_ts = beta_t rk_t rk_s e^{G_t-G_s} (K K^T)_ts, s < t
-//                                             P_ts = rq_t rk_s e^{G_t-G_s} (Q K^T)_ts,         s <= t
-//   solve: T = (I + A)^-1                  (blocked forward substitution, fp32, CUDA cores)
-//          PT = P T                        (tensor cores)
-//   chain: [Y; Y_q] = [K; Q] S^T           Z = diag(beta) (V - diag(e rk) Y)
-//          [U; O_p] = [T; PT] Z            (so U = T diag(beta) V - T diag(beta e rk) K S^T,
-//                                           O_p = P U)
-//          O   = diag(e rq) Y_q + O_p      -> out (bf16)
-//          S^T <- gamma S^T + K^T diag(d rk) U
-// The raw K, Q, V tiles enter the MMAs exactly (bf16); every computed operand
-// (S, T, PT, P, Z, U) is split into bf16 hi + lo parts and multiplied as
-// hi*hi + hi*lo + lo*hi (or raw*hi + raw*lo), so each product keeps about
-// 16 significant bits while the accumulation is fp32 in TMEM. The state itself
-// stays in fp32 registers (thread j holds column j of S) and is never rounded.
+//   A_ts = beta_t e^{G_t-G_s} kh_t.kh_s (s < t),  P_ts = e^{G_t-G_s} qh_t.kh_s (s <= t)
+//   T  = (I + A)^-1,  Tb = T diag(beta),  Tw = T diag(beta e)
+//   W  = Tw Kh                           (C x dk)
+//   U^T = V^T Tb^T - S W^T               (dv x C)      <- first state-dependent product
+//   S  <- gamma S + U^T diag(d) Kh       (dv x dk)     <- second state-dependent product
+//   O^T = S Qh^T diag(e) + U^T P^T       (dv x C)
+// The state product is transposed so that the 128 state rows sit on the 128 TMEM
+// lanes: one thread owns one row of S in fp32 registers for the whole sequence,
+// and an fp16 copy of S is the A operand of the MMAs straight from TMEM.
 //
-// Rows t >= L of a partial block have beta = 0, rk = rq = 0 and d = 0, so they
-// contribute nothing; their outputs are not stored.
+// Work split (512 threads = two groups of 8 warps, two warps per scheduler):
+//   * threads 0..255, "prep", run one block ahead: TMA of the raw K, Q, V tiles,
+//     norms and gates, fp16 conversion, the Gram MMA, A and P, the blocked
+//     triangular solve on CUDA cores, W by MMA, then hands the block's operands
+//     over in one of two shared-memory stages;
+//   * threads 256..511, "chain", own the state (each thread half a row): per block two MMA round trips
+//     (U^T, then the state update) plus the output products.
+// Each group issues its own MMAs from one thread; stages are handed over with
+// mbarriers (full / empty), MMA completion is tracked with tcgen05.commit.
+//
+// Numerics: every MMA multiplies fp16 operands into fp32 accumulators. Each
+// operand is scaled by an exact power of two before rounding to fp16 (per block
+// for V, Tb, Tw, W and P from their maxima; per row of S and U in the chain, so
+// no cross-thread reduction), which keeps every value in fp16's normal range and
+// each product to about 2^-11 relative. Raw q/k are normalised before rounding.
+//
+// Rows t >= L of a partial block get zero kh, qh, beta, d, so they contribute
+// nothing; their outputs are not stored.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -42,37 +53,59 @@ namespace {
 
 using namespace tc;
 
-constexpr int C = 64;       // block length
-constexpr int DK = 128;     // key dim
-constexpr int DV = 128;     // value dim
-constexpr int kThreads = 128;
+constexpr int C = 64;     // block length
+constexpr int DK = 128;   // key dim
+constexpr int DV = 128;   // value dim
+constexpr int kThreads = 512;
+constexpr int kWG = 256;  // threads per warpgroup pair ("prep" 0..255, "chain" 256..511)
 constexpr long long kWaitBudget = 4000000000LL;  // SM cycles (about 2 s) before a wait gives up
 
-// shared memory map, byte offsets from a 1 KiB aligned base
-constexpr uint32_t OFF_KQ = 0;        // 32 KiB [kb 0..1][rows: K 0..63 | Q 64..127][128 B], TMA
-constexpr uint32_t OFF_V = 32768;     // 16 KiB [kb 0..1][t 0..63][128 B], TMA
-constexpr uint32_t OFF_SHI = 49152;   // 32 KiB S hi, MN-major [i-block 0..1][j 0..127][128 B]
-constexpr uint32_t OFF_SLO = 81920;   // 32 KiB S lo
-constexpr uint32_t OFF_PHI = 114688;  // 16 KiB P hi, K-major [t 0..127][128 B] (rows 64.. zero)
-constexpr uint32_t OFF_PLO = 131072;  // 16 KiB P lo
-constexpr uint32_t OFF_THI = 147456;  // 16 KiB [T; PT] hi, K-major [t 0..127][128 B]
-constexpr uint32_t OFF_TLO = 163840;  // 16 KiB [T; PT] lo
-constexpr uint32_t OFF_Z = 180224;    // 36 KiB: Z / U~ hi (16 KiB) + lo (16 KiB), MN-major
-                                      //         [i-block 0..1][t 0..63][128 B];
-                                      //         during the solve: A, T fp32 [64][64] + scratch
-constexpr uint32_t OFF_SC = 217088;   // per-token scalars, 6 x 64 fp32
-constexpr uint32_t OFF_BAR = OFF_SC + 6 * 64 * 4;
-constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+// ---- shared memory map (byte offsets from a 1 KiB aligned base) ----
+// operand stage s (two of them), handed from prep to chain
+constexpr uint32_t ST_KQ = 0;       // 32 KiB [kb 0..1][rows: Kh 0..63 | Qh 64..127][128 B] fp16
+constexpr uint32_t ST_V = 32768;    // 16 KiB [i-block 0..1][t 0..63][128 B] fp16, scaled V
+constexpr uint32_t ST_TB = 49152;   //  8 KiB [t][s] fp16, scaled Tb           } fp32 T during the solve
+constexpr uint32_t ST_P = 57344;    //  8 KiB [t][s] fp16, scaled P            }
+constexpr uint32_t ST_W = 65536;    // 16 KiB MN-major [j 0..127][64 t] fp16, scaled -W; fp32 A during the solve
+constexpr uint32_t ST_SC = 81920;   //  1 KiB block scalars (below)
+constexpr uint32_t STAGE = 82944;
+// stage scalars (float index)
+constexpr int SC_D = 0, SC_E = 64, SC_GAMMA = 128, SC_X1 = 129, SC_X2 = 130, SC_PO = 131, SC_L = 132;
+// prep-private
+constexpr uint32_t RAW = 2 * STAGE;   // 48 KiB raw bf16 tiles: K (0, 8K), Q (16K, 24K), V (32K, 40K)
+constexpr uint32_t TW = RAW + 49152;  //  8 KiB [t][s] fp16, scaled Tw; solve scratch X before
+constexpr uint32_t PSC = TW + 8192;   // prep scalars (float index below)
+constexpr int PS_G = 0, PS_BETA = 64, PS_AA = 128, PS_BB = 192, PS_EE = 256, PS_BE = 320, PS_DD = 384,
+              PS_SS = 448 /* [2][128] */, PS_FACT = 704, PS_RED = 712 /* [sites][8 warps][4] */;
+constexpr int RED_V = 0, RED_TP = 1, RED_W = 2;  // reduction sites
+constexpr uint32_t CSC = PSC + 4 * (PS_RED + 3 * 32);  // chain scratch: [2 sites][2 halves][128] floats
+constexpr uint32_t BAR = CSC + 4 * 512;
+constexpr uint32_t SMEM_USED = BAR + 128;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
 static_assert(SMEM_BYTES <= 232448, "over the 227 KiB opt-in limit");
 
-// TMEM columns (512 allocated): Gram / PT, [Y; Y_q], [U; O_p], K^T U~
-constexpr uint32_t TM_G = 0, TM_Y = 64, TM_U = 192, TM_S = 320;
+// ---- TMEM columns (512 allocated) ----
+constexpr uint32_t TM_GW = 0;     // prep: Gram, then W^T          (64)
+constexpr uint32_t TM_X1 = 64;    // chain: V^T Tb^T               (64)
+constexpr uint32_t TM_X2 = 128;   // chain: S (-W)^T, then U^T P^T (64)
+constexpr uint32_t TM_Q = 192;    // chain: S Qh^T                 (64)
+constexpr uint32_t TM_S = 256;    // chain: U~^T Kh                (128)
+constexpr uint32_t TM_AS = 384;   // chain: fp16 S, A operand      (64 = 128 fp16)
+constexpr uint32_t TM_AUT = 448;  // chain: fp16 U^T diag(d)       (32)
+constexpr uint32_t TM_AU = 480;   // chain: fp16 U^T               (32)
 
-constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);        // Gram
-constexpr uint32_t ID_N64_BMN = idesc_bf16(128, 64, 0, 1);    // PT
-constexpr uint32_t ID_N128_BMN = idesc_bf16(128, 128, 0, 1);  // Y, U
-constexpr uint32_t ID_N128_AMN_BMN = idesc_bf16(128, 128, 1, 1);  // K^T U~
+// instruction descriptor, kind::f16 with fp16 operands and an fp32 accumulator
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t ID_GRAM = idesc_f16(128, 64, 0, 0);
+constexpr uint32_t ID_W = idesc_f16(128, 64, 1, 0);
+constexpr uint32_t ID_X1 = idesc_f16(128, 64, 1, 0);
+constexpr uint32_t ID_X2 = idesc_f16(128, 64, 0, 1);
+constexpr uint32_t ID_Q = idesc_f16(128, 64, 0, 0);
+constexpr uint32_t ID_S = idesc_f16(128, 128, 0, 1);
+constexpr uint32_t ID_O = idesc_f16(128, 64, 0, 0);
 
 struct TcParams {
     const __nv_bfloat16 *g, *b;
@@ -85,416 +118,635 @@ struct TcParams {
     int *status;
 };
 
-// T = (I + A)^-1 for a unit lower-triangular 64 x 64 matrix, A strictly lower, row-major fp32.
-// Diagonal 16 x 16 blocks by forward substitution (one column per thread), then the
-// off-diagonal blocks by block diagonals: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
-__device__ void solve_unit_lower(const float *sA, float *sT, float *sX, int tid) {
-    if (tid < 64) {
-        const int b = tid >> 4, c = tid & 15;
+// ---- small helpers ----
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    mma_bf16(d, a, b, idesc, acc);  // same instruction; the operand type is in the idesc
+}
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// 32 lanes x 16 consecutive columns
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t h2_bits(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint4 pack8_f16(const float *x, float s) {
+    return make_uint4(h2_bits(s * x[0], s * x[1]), h2_bits(s * x[2], s * x[3]), h2_bits(s * x[4], s * x[5]),
+                      h2_bits(s * x[6], s * x[7]));
+}
+// exact power of two 2^(14 - e) with m < 2^e: m * scale < 2^14 (fp16 max 65504)
+__device__ __forceinline__ float pow2_scale(float m) {
+    if (!(m > 0.f) || !isfinite(m)) return 1.f;
+    int e;
+    frexpf(m, &e);
+    e = max(-100, min(100, 14 - e));
+    return ldexpf(1.f, e);
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+// fp32 64 x 64 row-major with the column index XOR-swizzled by the row (keeps float4 groups)
+__device__ __forceinline__ int sw(int t, int s) { return t * 64 + (s ^ ((t & 7) << 2)); }
+
+// T = (I + A)^-1, A strictly lower 64 x 64 (swizzled fp32); 256 threads of one warpgroup pair.
+// Diagonal 16 x 16 blocks by forward substitution (one column per thread), then the block
+// diagonals T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, each thread owning 4 adjacent outputs.
+__device__ void solve_unit_lower(const float *sA, float *sT, float *sX, int p, int bar_id) {
+    if (p < 64) {
+        const int b = p >> 4, c = p & 15;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             float acc = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc -= sA[(16 * b + r) * 64 + 16 * b + s] * x[s];
+            for (int s = 0; s < r; ++s) acc -= sA[sw(16 * b + r, 16 * b + s)] * x[s];
             x[r] = acc;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(16 * b + r) * 64 + 16 * b + c] = x[r];
+        for (int r = 0; r < 16; ++r) sT[sw(16 * b + r, 16 * b + c)] = x[r];
         for (int i = 0; i < b; ++i)
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(16 * i + r) * 64 + 16 * b + c] = 0.f;
+            for (int r = 0; r < 16; ++r) sT[sw(16 * i + r, 16 * b + c)] = 0.f;
     }
-    __syncthreads();
+    bar_sync(bar_id, kWG);
     for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;
-        for (int e = tid; e < nb * 256; e += kThreads) {
-            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int i = d + blk, j = blk;
-            float acc = 0.f;
-            for (int k = j; k < i; ++k)
+        const bool act = p < (4 - d) * 64;
+        const int blk = p >> 6, r = (p >> 2) & 15, c0 = (p & 3) * 4;
+        const int i = d + blk, j = blk;
+        if (act) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = j; k < i; ++k) {
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc += sA[(16 * i + r) * 64 + 16 * k + m] * sT[(16 * k + m) * 64 + 16 * j + c];
-            sX[e] = acc;
+                for (int m = 0; m < 16; ++m) {
+                    const float a = sA[sw(16 * i + r, 16 * k + m)];
+                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + sw(16 * k + m, 16 * j + c0));
+                    acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                }
+            }
+            *reinterpret_cast<float4 *>(sX + blk * 256 + r * 16 + c0) = acc;
         }
-        __syncthreads();
-        for (int e = tid; e < nb * 256; e += kThreads) {
-            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int i = d + blk, j = blk;
-            float acc = 0.f;
+        bar_sync(bar_id, kWG);
+        if (act) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc += sT[(16 * i + r) * 64 + 16 * i + m] * sX[(blk << 8) + (m << 4) + c];
-            sT[(16 * i + r) * 64 + 16 * j + c] = -acc;
+            for (int m = 0; m < 16; ++m) {
+                const float a = sT[sw(16 * i + r, 16 * i + m)];
+                const float4 x4 = *reinterpret_cast<const float4 *>(sX + blk * 256 + m * 16 + c0);
+                acc.x += a * x4.x; acc.y += a * x4.y; acc.z += a * x4.z; acc.w += a * x4.w;
+            }
+            *reinterpret_cast<float4 *>(sT + sw(16 * i + r, 16 * j + c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
-        __syncthreads();
+        bar_sync(bar_id, kWG);
     }
-}
-
-// S (thread j holds S[:, j]) -> hi/lo bf16, MN-major B operand rows j
-__device__ __forceinline__ void store_state_hilo(uint8_t *sm, int j, const float (&S)[DV]) {
-#pragma unroll
-    for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 hi, lo;
-            pack8_hilo(&S[mb * 64 + 8 * c], hi, lo);
-            *reinterpret_cast<uint4 *>(sm + OFF_SHI + mb * 16384 + swz(j, c)) = hi;
-            *reinterpret_cast<uint4 *>(sm + OFF_SLO + mb * 16384 + swz(j, c)) = lo;
-        }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sb = smem_u32(sm);
-    float *rk_s = reinterpret_cast<float *>(sm + OFF_SC);
-    float *rq_s = rk_s + 64, *beta_s = rq_s + 64, *G_s = beta_s + 64, *eG_s = G_s + 64, *dG_s = eG_s + 64;
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *bar_mma = bar_tma + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
-    int *abort_s = reinterpret_cast<int *>(tmem_slot + 1);
-    float *sA = reinterpret_cast<float *>(sm + OFF_Z);
-    float *sT = sA + 64 * 64;
-    float *sX = sT + 64 * 64;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
+    uint64_t *bar_tma = bars + 0, *bar_prep = bars + 1, *bar_full = bars + 2, *bar_empty = bars + 4;
+    uint64_t *bar_x = bars + 6, *bar_q = bars + 7, *bar_s = bars + 8, *bar_o = bars + 9;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
+    // one abort flag per warpgroup pair, written only by its own threads and read after its own barriers
+    volatile int *abort_p = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *abort_c = abort_p + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x, n = blockIdx.y;
     const int hk = h / (p.Hv / p.Hk);
     long bos, eos;
     if (!seq_bounds(p.cu, n, p.B, p.cu ? p.Ttot : p.T, &bos, &eos, p.status)) return;
+    const int nchunks = (int)((eos - bos + C - 1) / C);
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_prep, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_full + s, 1);
+            mbar_init(bar_empty + s, 1);
+        }
+        mbar_init(bar_x, 1);
+        mbar_init(bar_q, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
         fence_mbar_init();
-        *abort_s = 0;
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
+        *abort_p = 0;
+        *abort_c = 0;
     }
     if (warp == 0) tmem_alloc(tmem_slot, 512);
-    {  // rows 64..127 of the P operand stay zero
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = tid; i < 512; i += kThreads) {
-            reinterpret_cast<uint4 *>(sm + OFF_PHI + 8192)[i] = z;
-            reinterpret_cast<uint4 *>(sm + OFF_PLO + 8192)[i] = z;
-        }
-    }
-    float S[DV];  // column tid of the state
-    const long st_off = ((long)n * p.Hv + h) * (long)DV * DK;
-#pragma unroll
-    for (int i = 0; i < DV; ++i) S[i] = p.state_in ? p.state_in[st_off + (long)i * DK + tid] : 0.f;
-    store_state_hilo(sm, tid, S);
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    uint32_t ph_tma = 0, ph_mma = 0;
-    bool aborted = false;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
+    const int half = (tid >> 7) & 1;                              // which half of a row this thread owns
+    const int r = tid & 127;                                      // TMEM lane = row
 
-    auto wait_mma = [&]() {
-        if (!mbar_wait(bar_mma, ph_mma, kWaitBudget)) *abort_s = 1;
-        ph_mma ^= 1;
-        tc_fence_after();
-    };
-    auto sync_for_mma = [&]() {  // make generic smem writes and TMEM reads visible before an MMA
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-    };
-
-    for (long c0 = bos; c0 < eos; c0 += C) {
-        const int L = (int)min((long)C, eos - c0);
-        if (tid == 0) {
+    if (tid < kWG) {
+        // ======================= prep =======================
+        const int pt = tid;
+        float *ps = reinterpret_cast<float *>(sm + PSC);
+        float *red = ps + PS_RED;
+        uint32_t ph_prep = 0;
+        auto issue_tma = [&](int c_tok) {
             mbar_expect_tx(bar_tma, 6 * 8192);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-                tma_load_3d(sm + OFF_KQ + kb * 16384, &tm_k, kb * 64, hk, (int)c0, bar_tma);
-                tma_load_3d(sm + OFF_KQ + kb * 16384 + 8192, &tm_q, kb * 64, hk, (int)c0, bar_tma);
-                tma_load_3d(sm + OFF_V + kb * 8192, &tm_v, kb * 64, h, (int)c0, bar_tma);
+                tma_load_3d(sm + RAW + kb * 8192, &tm_k, kb * 64, hk, c_tok, bar_tma);
+                tma_load_3d(sm + RAW + 16384 + kb * 8192, &tm_q, kb * 64, hk, c_tok, bar_tma);
+                tma_load_3d(sm + RAW + 32768 + kb * 8192, &tm_v, kb * 64, h, c_tok, bar_tma);
             }
+        };
+        if (pt == 0 && nchunks > 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            issue_tma((int)bos);
         }
-        if (tid < C) {
-            const bool ok = tid < L;
-            G_s[tid] = ok ? to_f32(p.g[(c0 + tid) * p.Hv + h]) : 0.f;
-            beta_s[tid] = ok ? sigmoidf_(to_f32(p.b[(c0 + tid) * p.Hv + h])) : 0.f;
+        float g_nx = 0.f, b_nx = 0.f;  // gates of the next block, fetched one block ahead
+        if (pt < C && nchunks > 0 && pt < eos - bos) {
+            g_nx = to_f32(p.g[(bos + pt) * p.Hv + h]);
+            b_nx = to_f32(p.b[(bos + pt) * p.Hv + h]);
         }
-        if (!mbar_wait(bar_tma, ph_tma, kWaitBudget)) *abort_s = 1;
-        ph_tma ^= 1;
-        __syncthreads();
-        if (*abort_s) { aborted = true; break; }
-
-        // inverse norms: warps 0-1 the K rows, warps 2-3 the Q rows
-        {
-            const int t = tid & 63;
-            const uint32_t base = OFF_KQ + (tid >= 64 ? 8192u : 0u);
-            float ss = 0.f;
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float x[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(sm + base + kb * 16384 + swz(t, c)), x);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+        for (int k = 0; k < nchunks; ++k) {
+            const long c0 = bos + (long)k * C;
+            const int L = (int)min((long)C, eos - c0);
+            const int s = k & 1;
+            uint8_t *st = sm + s * STAGE;
+            const uint32_t stb = sb + s * STAGE;
+            float *stsc = reinterpret_cast<float *>(st + ST_SC);
+            float *sA = reinterpret_cast<float *>(st + ST_W);
+            float *sT = reinterpret_cast<float *>(st + ST_TB);
+            float *sX = reinterpret_cast<float *>(sm + TW);
+            if (pt < C) {
+                ps[PS_G + pt] = pt < L ? g_nx : 0.f;
+                ps[PS_BETA + pt] = pt < L ? sigmoidf_(b_nx) : 0.f;
+                const long cn = c0 + C + pt;
+                if (k + 1 < nchunks && cn < eos) {
+                    g_nx = to_f32(p.g[cn * p.Hv + h]);
+                    b_nx = to_f32(p.b[cn * p.Hv + h]);
                 }
-            (tid >= 64 ? rq_s : rk_s)[t] = t < L ? rsqrtf(ss + kNormEps) : 0.f;
-        }
-        if (warp == 0) {  // in-block inclusive cumulative log-gate
-            float x0 = G_s[lane], x1 = G_s[lane + 32];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-                const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-                if (lane >= o) { x0 += y0; x1 += y1; }
             }
-            x1 += __shfl_sync(0xffffffffu, x0, 31);
-            G_s[lane] = x0;
-            G_s[lane + 32] = x1;
-        }
-        __syncthreads();
-        const float GL = G_s[L - 1];
-        if (tid < C) {
-            eG_s[tid] = expf(G_s[tid]);
-            dG_s[tid] = tid < L ? expf(GL - G_s[tid]) : 0.f;
-        }
-
-        // ---- Gram: [K; Q] K^T ----
-        if (tid == 0) {
+            if (!mbar_wait(bar_tma, k & 1, kWaitBudget)) *abort_p = 1;
+            bar_sync(1, kWG);
+            if (*abort_p) break;
+            // ---- row norms (half a row per thread), V maximum; warp 0 also scans the gates ----
+            const int row = r & 63;  // K rows for r < 64, Q rows for r >= 64
+            const uint32_t raw_row = RAW + (r >= 64 ? 16384u : 0u) + half * 8192;
+            uint4 raw8[8];
+            float ssq = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                raw8[c] = *reinterpret_cast<const uint4 *>(sm + raw_row + swz(row, c));
+                float x[8];
+                unpack8(raw8[c], x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ssq += x[e] * x[e];
+            }
+            ps[PS_SS + half * 128 + r] = ssq;
+            const int vt = pt >> 2, vq = (pt & 3) * 4;  // V: row vt, chunks vq..vq+3 of 16
+            uint4 rawv[4];
+            float vmax = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = vq + cc;
+                rawv[cc] = *reinterpret_cast<const uint4 *>(sm + RAW + 32768 + (c >> 3) * 8192 + swz(vt, c & 7));
+                float x[8];
+                unpack8(rawv[cc], x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vmax = fmaxf(vmax, fabsf(x[e]));
+            }
+            vmax = warp_max(vt < L ? vmax : 0.f);
+            if (lane == 0) red[RED_V * 32 + warp * 4] = vmax;
+            if (warp == 0) {
+                float x0 = ps[PS_G + lane], x1 = ps[PS_G + lane + 32];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+                    const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+                    if (lane >= o) { x0 += y0; x1 += y1; }
+                }
+                x1 += __shfl_sync(0xffffffffu, x0, 31);
+                ps[PS_G + lane] = x0;
+                ps[PS_G + lane + 32] = x1;
+            }
+            bar_sync(1, kWG);
+            const float GL = ps[PS_G + L - 1];
+            const float rnorm = row < L ? rsqrtf(ps[PS_SS + r] + ps[PS_SS + 128 + r] + kNormEps) : 0.f;
+            float vm = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) vm = fmaxf(vm, red[RED_V * 32 + w * 4]);
+            const float sig_v = pow2_scale(vm);
+            if (pt < C) {  // per-token exp factors, computed once
+                float gmin = ps[PS_G], gmax = ps[PS_G];
+#pragma unroll 8
+                for (int t = 1; t < C; ++t) {
+                    gmin = fminf(gmin, ps[PS_G + t]);
+                    gmax = fmaxf(gmax, ps[PS_G + t]);
+                }
+                const float G = ps[PS_G + pt];
+                ps[PS_AA + pt] = expf(G - gmin);
+                ps[PS_BB + pt] = expf(gmin - G);
+                const float e = expf(G);
+                ps[PS_EE + pt] = e;
+                ps[PS_BE + pt] = ps[PS_BETA + pt] * e;
+                ps[PS_DD + pt] = pt < L ? expf(GL - G) : 0.f;
+                if (pt == 0) ps[PS_FACT] = (gmax - gmin) < 80.f ? 1.f : 0.f;  // a_t b_s = e^{G_t-G_s} safely
+            }
+            // ---- wait until the chain released this stage (block k-2), then write fp16 operands ----
+            if (k >= 2 && !mbar_wait(bar_empty + s, ((k - 2) >> 1) & 1, kWaitBudget)) *abort_p = 1;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float x[8];
+                unpack8(raw8[c], x);
+                *reinterpret_cast<uint4 *>(st + ST_KQ + half * 16384 + swz(r, c)) = pack8_f16(x, rnorm);
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = vq + cc;
+                float x[8];
+                unpack8(rawv[cc], x);
+                *reinterpret_cast<uint4 *>(st + ST_V + (c >> 3) * 8192 + swz(vt, c & 7)) =
+                    pack8_f16(x, vt < L ? sig_v : 0.f);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            bar_sync(1, kWG);
+            if (*abort_p) break;
+            if (pt == 0) {
+                if (k + 1 < nchunks) issue_tma((int)(c0 + C));  // raw tiles consumed: fetch the next block
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {  // Gram [Kh; Qh] Kh^T
+                    const uint64_t d = desc_sw128(stb + ST_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                    mma_f16_ss(tmem + TM_GW, d, d, ID_GRAM, ks > 0);
+                }
+                mma_commit(bar_prep);
+            }
+            if (!mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;
+            ph_prep ^= 1;
             tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16(tmem + TM_G, desc_sw128(sb + off, 16, 1024), desc_sw128(sb + off, 16, 1024), ID_N64, s > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-        __syncthreads();
-        if (*abort_s) { aborted = true; break; }
-
-        // ---- A (fp32, for the solve) and P (hi/lo operand) ----
-        {
-            const int t = tid & 63;
-            float row[64];
+            // ---- A rows (fp32, swizzled, for the solve); P rows stay in registers ----
+            const bool factor = ps[PS_FACT] != 0.f;
+            float pv[32];
+            float mp = 0.f;
             {
-                float v0[32], v1[32];
-                tmem_ld32(tmem + TM_G + lane_off, v0);
-                tmem_ld32(tmem + TM_G + lane_off + 32, v1);
+                float v0[16], v1[16];
+                tmem_ld16(tmem + TM_GW + lane_off + 32 * half, v0);
+                tmem_ld16(tmem + TM_GW + lane_off + 32 * half + 16, v1);
+                const float at = ps[PS_AA + row], Gt = ps[PS_G + row];
+                const float bt = r < 64 ? ps[PS_BETA + row] * at : at;
+                if (factor) {  // uniform branch: e^{G_t-G_s} = a_t b_s
 #pragma unroll
-                for (int s = 0; s < 32; ++s) { row[s] = v0[s]; row[32 + s] = v1[s]; }
-            }
-            const float Gt = G_s[t];
-            if (tid < 64) {
-                const float bt = beta_s[t] * rk_s[t];
+                    for (int e = 0; e < 32; ++e) pv[e] = (e < 16 ? v0[e] : v1[e - 16]) * bt * ps[PS_BB + 32 * half + e];
+                } else {
+                    const float bb = r < 64 ? ps[PS_BETA + row] : 1.f;
 #pragma unroll
-                for (int s = 0; s < 64; ++s) {
-                    const float a = bt * rk_s[s] * expf(Gt - G_s[s]) * row[s];
-                    sA[t * 64 + s] = s < t ? a : 0.f;
+                    for (int e = 0; e < 32; ++e)
+                        pv[e] = (e < 16 ? v0[e] : v1[e - 16]) * bb * expf(Gt - ps[PS_G + 32 * half + e]);
                 }
-            } else {
-                const float qt = rq_s[t];
+                if (r < 64) {
 #pragma unroll
-                for (int s = 0; s < 64; ++s) {
-                    const float pv = qt * rk_s[s] * expf(Gt - G_s[s]) * row[s];
-                    row[s] = s <= t ? pv : 0.f;
-                }
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const int s2 = 32 * half + 4 * e4;
+                        float4 a4;
+                        a4.x = s2 + 0 < row ? pv[4 * e4 + 0] : 0.f;
+                        a4.y = s2 + 1 < row ? pv[4 * e4 + 1] : 0.f;
+                        a4.z = s2 + 2 < row ? pv[4 * e4 + 2] : 0.f;
+                        a4.w = s2 + 3 < row ? pv[4 * e4 + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(sA + sw(row, s2)) = a4;
+                    }
+                } else {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 hi, lo;
-                    pack8_hilo(&row[8 * c], hi, lo);
-                    *reinterpret_cast<uint4 *>(sm + OFF_PHI + swz(t, c)) = hi;
-                    *reinterpret_cast<uint4 *>(sm + OFF_PLO + swz(t, c)) = lo;
-                }
-            }
-        }
-        __syncthreads();
-
-        // ---- T = (I + A)^-1, rows 0..63 of the [T; PT] operand ----
-        solve_unit_lower(sA, sT, sX, tid);
-        if (tid < 64) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 hi, lo;
-                pack8_hilo(&sT[tid * 64 + 8 * c], hi, lo);
-                *reinterpret_cast<uint4 *>(sm + OFF_THI + swz(tid, c)) = hi;
-                *reinterpret_cast<uint4 *>(sm + OFF_TLO + swz(tid, c)) = lo;
-            }
-        }
-        sync_for_mma();
-
-        // ---- PT = P T (B = T rows as an MN-major operand) ----
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t a_op[3] = {OFF_PHI, OFF_PHI, OFF_PLO}, b_op[3] = {OFF_THI, OFF_TLO, OFF_THI};
-            int first = 1;
-#pragma unroll
-            for (int m = 0; m < 3; ++m)
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    mma_bf16(tmem + TM_G, desc_sw128(sb + a_op[m] + s * 32, 16, 1024),
-                             desc_sw128(sb + b_op[m] + s * 2048, 8192, 1024), ID_N64_BMN, !first);
-                    first = 0;
-                }
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-        if (tid < 64) {  // rows 64..127 of [T; PT]
-            float v0[32], v1[32];
-            tmem_ld32(tmem + TM_G + lane_off, v0);
-            tmem_ld32(tmem + TM_G + lane_off + 32, v1);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 hi, lo;
-                pack8_hilo(c < 4 ? &v0[8 * c] : &v1[8 * (c - 4)], hi, lo);
-                *reinterpret_cast<uint4 *>(sm + OFF_THI + swz(64 + tid, c)) = hi;
-                *reinterpret_cast<uint4 *>(sm + OFF_TLO + swz(64 + tid, c)) = lo;
-            }
-        }
-        sync_for_mma();
-        if (*abort_s) { aborted = true; break; }
-
-        // ---- [Y; Y_q] = [K; Q] S^T ----
-        if (tid == 0) {
-            tc_fence_after();
-            int first = 1;
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t a_off = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
-                    const uint32_t b_off = (m == 0 ? OFF_SHI : OFF_SLO) + s * 2048;
-                    mma_bf16(tmem + TM_Y, desc_sw128(sb + a_off, 16, 1024), desc_sw128(sb + b_off, 16384, 1024),
-                             ID_N128_BMN, !first);
-                    first = 0;
-                }
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-        // ---- Z = diag(beta) (V - diag(e rk) Y), rows t (warps 0-1) ----
-        if (tid < 64) {
-            const int t = tid;
-            const float bt = beta_s[t], et = eG_s[t] * rk_s[t];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float y[32];
-                tmem_ld32(tmem + TM_Y + lane_off + 32 * q4, y);
-                const int kb = q4 >> 1;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = (q4 & 1) * 4 + cc;
-                    float v8[8], z[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_V + kb * 8192 + swz(t, c)), v8);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) z[e] = bt * (v8[e] - et * y[cc * 8 + e]);
-                    uint4 hi, lo;
-                    pack8_hilo(z, hi, lo);
-                    *reinterpret_cast<uint4 *>(sm + OFF_Z + kb * 8192 + swz(t, c)) = hi;
-                    *reinterpret_cast<uint4 *>(sm + OFF_Z + 16384 + kb * 8192 + swz(t, c)) = lo;
-                }
-            }
-        }
-        sync_for_mma();
-
-        // ---- [U; O_p] = [T; PT] Z ----
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t a_op[3] = {OFF_THI, OFF_THI, OFF_TLO}, b_op[3] = {OFF_Z, OFF_Z + 16384, OFF_Z};
-            int first = 1;
-#pragma unroll
-            for (int m = 0; m < 3; ++m)
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    mma_bf16(tmem + TM_U, desc_sw128(sb + a_op[m] + s * 32, 16, 1024),
-                             desc_sw128(sb + b_op[m] + s * 2048, 8192, 1024), ID_N128_BMN, !first);
-                    first = 0;
-                }
-            mma_commit(bar_mma);
-        }
-        wait_mma();
-        if (tid < 64) {
-            // U~ = diag(d rk) U, hi/lo, over the consumed Z operand
-            const int t = tid;
-            const float sc = dG_s[t] * rk_s[t];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float u[32];
-                tmem_ld32(tmem + TM_U + lane_off + 32 * q4, u);
-                const int kb = q4 >> 1;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = (q4 & 1) * 4 + cc;
-                    float z[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) z[e] = sc * u[cc * 8 + e];
-                    uint4 hi, lo;
-                    pack8_hilo(z, hi, lo);
-                    *reinterpret_cast<uint4 *>(sm + OFF_Z + kb * 8192 + swz(t, c)) = hi;
-                    *reinterpret_cast<uint4 *>(sm + OFF_Z + 16384 + kb * 8192 + swz(t, c)) = lo;
-                }
-            }
-        } else {
-            // O = diag(e rq) Y_q + O_p, rows t = tid - 64
-            const int t = tid - 64;
-            const float sc = eG_s[t] * rq_s[t];
-            __nv_bfloat16 *orow = p.out + ((c0 + t) * p.Hv + h) * (long)DV;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float yq[32], op[32];
-                tmem_ld32(tmem + TM_Y + lane_off + 32 * q4, yq);
-                tmem_ld32(tmem + TM_U + lane_off + 32 * q4, op);
-                if (t < L) {
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float o[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = sc * yq[cc * 8 + e] + op[cc * 8 + e];
-                        *reinterpret_cast<uint4 *>(orow + 32 * q4 + 8 * cc) = pack8(o);
+                    for (int e = 0; e < 32; ++e) {
+                        pv[e] = 32 * half + e <= row ? pv[e] : 0.f;
+                        mp = fmaxf(mp, fabsf(pv[e]));
                     }
                 }
             }
-        }
-        sync_for_mma();
-
-        // ---- S^T update: K^T U~ ----
-        if (tid == 0) {
-            tc_fence_after();
+            tc_fence_before();
+            bar_sync(1, kWG);
+            // ---- T = (I + A)^-1 ----
+            solve_unit_lower(sA, sT, sX, pt, 1);
+            // ---- Tb, Tw (thread: row t, 16 columns), P scale; one reduction round ----
+            const int tt = pt >> 2, q = pt & 3;
+            float tb[16], tw[16];
+            float mb = 0.f, mw = 0.f;
 #pragma unroll
-            for (int m = 0; m < 2; ++m)
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(sT + sw(tt, 16 * q + 4 * c4));
+                const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    mma_bf16(tmem + TM_S, desc_sw128(sb + OFF_KQ + s * 2048, 16384, 1024),
-                             desc_sw128(sb + OFF_Z + m * 16384 + s * 2048, 8192, 1024), ID_N128_AMN_BMN,
-                             (m | s) != 0);
+                for (int e = 0; e < 4; ++e) {
+                    const int s2 = 16 * q + 4 * c4 + e;
+                    tb[4 * c4 + e] = tv[e] * ps[PS_BETA + s2];
+                    tw[4 * c4 + e] = tv[e] * ps[PS_BE + s2];
+                    mb = fmaxf(mb, fabsf(tb[4 * c4 + e]));
+                    mw = fmaxf(mw, fabsf(tw[4 * c4 + e]));
                 }
-            mma_commit(bar_mma);
+            }
+            mb = warp_max(mb);
+            mw = warp_max(mw);
+            mp = warp_max(mp);
+            if (lane == 0) {
+                red[RED_TP * 32 + warp * 4 + 0] = mb;
+                red[RED_TP * 32 + warp * 4 + 1] = mw;
+                red[RED_TP * 32 + warp * 4 + 2] = mp;
+            }
+            bar_sync(1, kWG);  // also: every read of T is done before Tb and P overwrite it
+            float mbb = 0.f, mww = 0.f, mpp = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                mbb = fmaxf(mbb, red[RED_TP * 32 + w * 4 + 0]);
+                mww = fmaxf(mww, red[RED_TP * 32 + w * 4 + 1]);
+                mpp = fmaxf(mpp, red[RED_TP * 32 + w * 4 + 2]);
+            }
+            const float sig_b = pow2_scale(mbb), sig_w = pow2_scale(mww), sig_p = pow2_scale(mpp);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                *reinterpret_cast<uint4 *>(st + ST_TB + swz(tt, 2 * q + cc)) = pack8_f16(&tb[8 * cc], sig_b);
+                *reinterpret_cast<uint4 *>(sm + TW + swz(tt, 2 * q + cc)) = pack8_f16(&tw[8 * cc], sig_w);
+            }
+            if (r >= 64) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4 *>(st + ST_P + swz(row, 4 * half + cc)) = pack8_f16(&pv[8 * cc], sig_p);
+            }
+            fence_async_smem();
+            bar_sync(1, kWG);
+            // ---- W^T = Kh^T Tw^T (scaled by sig_w) ----
+            if (pt == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16_ss(tmem + TM_GW, desc_sw128(stb + ST_KQ + ks * 2048, 16384, 1024),
+                               desc_sw128(sb + TW + ks * 32, 16, 1024), ID_W, ks > 0);
+                mma_commit(bar_prep);
+            }
+            if (!mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;
+            ph_prep ^= 1;
+            tc_fence_after();
+            {  // thread (j = r, half): W^T row j over t in this half -> MN-major row j of the -W operand
+                float w0[16], w1[16];
+                tmem_ld16(tmem + TM_GW + lane_off + 32 * half, w0);
+                tmem_ld16(tmem + TM_GW + lane_off + 32 * half + 16, w1);
+                float m = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) m = fmaxf(m, fmaxf(fabsf(w0[e]), fabsf(w1[e])));
+                m = warp_max(m);
+                if (lane == 0) red[RED_W * 32 + warp * 4] = m;
+                bar_sync(1, kWG);
+                float mm = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) mm = fmaxf(mm, red[RED_W * 32 + w * 4]);
+                const float inv_w = 1.f / sig_w;
+                const float sig_ww = pow2_scale(mm * inv_w);
+                const float f = -sig_ww * inv_w;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    *reinterpret_cast<uint4 *>(st + ST_W + swz(r, 4 * half + cc)) = pack8_f16(&w0[8 * cc], f);
+                    *reinterpret_cast<uint4 *>(st + ST_W + swz(r, 4 * half + 2 + cc)) = pack8_f16(&w1[8 * cc], f);
+                }
+                if (pt < C) {
+                    stsc[SC_D + pt] = ps[PS_DD + pt];
+                    stsc[SC_E + pt] = ps[PS_EE + pt];
+                }
+                if (pt == 0) {
+                    stsc[SC_GAMMA] = expf(GL);
+                    stsc[SC_X1] = 1.f / (sig_v * sig_b);
+                    stsc[SC_X2] = 1.f / sig_ww;
+                    stsc[SC_PO] = 1.f / sig_p;
+                    reinterpret_cast<int *>(stsc)[SC_L] = L;
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            bar_sync(1, kWG);
+            if (pt == 0) mbar_arrive(bar_full + s);
         }
-        wait_mma();
-        {
-            const float gam = expf(GL);
+    } else {
+        // ======================= chain =======================
+        const int i = r;             // state row (TMEM lane)
+        const bool issuer = (tid == kWG);
+        float *cx = reinterpret_cast<float *>(sm + CSC);  // [2 sites][2 halves][128]
+        float S[64];                 // S[i][64 half .. 64 half + 63]
+        const long st_off = ((long)n * p.Hv + h) * (long)DV * DK + (long)i * DK + 64 * half;
+        if (p.state_in) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float d[32];
-                tmem_ld32(tmem + TM_S + lane_off + 32 * q4, d);
+            for (int j = 0; j < 64; j += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(p.state_in + st_off + j);
+                S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+            }
+        } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) S[32 * q4 + e] = gam * S[32 * q4 + e] + d[e];
+            for (int j = 0; j < 64; ++j) S[j] = 0.f;
+        }
+        // per-row power-of-two scale: both halves' maxima through shared memory
+        auto row_scale = [&](float m, int site) {
+            cx[site * 256 + half * 128 + i] = m;
+            bar_sync(2, kWG);
+            return pow2_scale(fmaxf(cx[site * 256 + i], cx[site * 256 + 128 + i]));
+        };
+        auto smax = [&]() {
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) m = fmaxf(m, fabsf(S[j]));
+            return m;
+        };
+        auto store_state_f16 = [&](float sc) {  // 64 values of row i -> 32 columns of the A operand
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                uint32_t rr[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) rr[c] = h2_bits(sc * S[16 * c8 + 2 * c], sc * S[16 * c8 + 2 * c + 1]);
+                tmem_st8(tmem + TM_AS + lane_off + 32 * half + 8 * c8, rr);
+            }
+        };
+        auto issue_x2q = [&](int k) {  // S(-W)^T and S Qh^T for block k
+            const uint32_t stb = sb + (k & 1) * STAGE;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_f16_ts(tmem + TM_X2, tmem + TM_AS + 8 * ks, desc_sw128(stb + ST_W + ks * 2048, 8192, 1024), ID_X2,
+                           ks > 0);
+            mma_commit(bar_x);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_f16_ts(tmem + TM_Q, tmem + TM_AS + 8 * ks,
+                           desc_sw128(stb + ST_KQ + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024), ID_Q, ks > 0);
+            mma_commit(bar_q);
+        };
+        auto issue_x1 = [&](int k) {  // V^T Tb^T for block k (state independent)
+            const uint32_t stb = sb + (k & 1) * STAGE;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ss(tmem + TM_X1, desc_sw128(stb + ST_V + ks * 2048, 8192, 1024),
+                           desc_sw128(stb + ST_TB + ks * 32, 16, 1024), ID_X1, ks > 0);
+        };
+
+        float sig_s = row_scale(smax(), 0);
+        if (nchunks > 0) {
+            if (!mbar_wait(bar_full + 0, 0, kWaitBudget)) *abort_c = 1;
+            store_state_f16(sig_s);
+            tmem_wait_st();
+            tc_fence_before();
+            bar_sync(2, kWG);
+            if (issuer && !*abort_c) {
+                tc_fence_after();
+                issue_x1(0);
+                issue_x2q(0);
             }
         }
-        store_state_hilo(sm, tid, S);
-        sync_for_mma();
-        if (*abort_s) { aborted = true; break; }
-    }
-
-    if (aborted) {
-        if (tid == 0) flag_error(p.status);
-    } else {
+        for (int k = 0; k < nchunks && !*abort_c; ++k) {
+            const long c0 = bos + (long)k * C;
+            const float *stsc = reinterpret_cast<const float *>(sm + (k & 1) * STAGE + ST_SC);
+            if (!mbar_wait(bar_full + (k & 1), (k >> 1) & 1, kWaitBudget)) *abort_c = 1;  // scalars of block k
+            // ---- E1: U^T = X1 / (sig_v sig_b) + X2 / (sig_s sig_ww) -> fp16 U~^T, U^T (columns t of this half) ----
+            if (!mbar_wait(bar_x, k & 1, kWaitBudget)) *abort_c = 1;
+            tc_fence_after();
+            const float f1 = stsc[SC_X1], f2 = stsc[SC_X2] / sig_s;
+            float m = 0.f;
 #pragma unroll
-        for (int i = 0; i < DV; ++i) p.state_out[st_off + (long)i * DK + tid] = S[i];
+            for (int q = 0; q < 2; ++q) {
+                float a[16], bx[16];
+                tmem_ld16(tmem + TM_X1 + lane_off + 32 * half + 16 * q, a);
+                tmem_ld16(tmem + TM_X2 + lane_off + 32 * half + 16 * q, bx);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    m = fmaxf(m, fabsf(a[e] * f1 + bx[e] * f2) * fmaxf(1.f, stsc[SC_D + 32 * half + 16 * q + e]));
+            }
+            const float sig_u = row_scale(m, 1);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float a[16], bx[16];
+                tmem_ld16(tmem + TM_X1 + lane_off + 32 * half + 16 * q, a);
+                tmem_ld16(tmem + TM_X2 + lane_off + 32 * half + 16 * q, bx);
+                uint32_t rd[8], ru[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int t0 = 32 * half + 16 * q + 2 * c;
+                    const float u0 = sig_u * (a[2 * c] * f1 + bx[2 * c] * f2);
+                    const float u1 = sig_u * (a[2 * c + 1] * f1 + bx[2 * c + 1] * f2);
+                    rd[c] = h2_bits(u0 * stsc[SC_D + t0], u1 * stsc[SC_D + t0 + 1]);
+                    ru[c] = h2_bits(u0, u1);
+                }
+                tmem_st8(tmem + TM_AUT + lane_off + 16 * half + 8 * q, rd);
+                tmem_st8(tmem + TM_AU + lane_off + 16 * half + 8 * q, ru);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            bar_sync(2, kWG);
+            if (*abort_c) break;
+            if (issuer) {
+                tc_fence_after();
+                const uint32_t stb = sb + (k & 1) * STAGE;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)  // U~^T Kh  (B = Kh rows, MN-major)
+                    mma_f16_ts(tmem + TM_S, tmem + TM_AUT + 8 * ks, desc_sw128(stb + ST_KQ + ks * 2048, 16384, 1024),
+                               ID_S, ks > 0);
+                mma_commit(bar_s);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)  // U^T P^T
+                    mma_f16_ts(tmem + TM_X2, tmem + TM_AU + 8 * ks, desc_sw128(stb + ST_P + ks * 32, 16, 1024), ID_O,
+                               ks > 0);
+                mma_commit(bar_o);
+            }
+            // ---- E2: state update (columns j of this half), next A operand, outputs ----
+            if (!mbar_wait(bar_s, k & 1, kWaitBudget)) *abort_c = 1;
+            tc_fence_after();
+            const float gam = stsc[SC_GAMMA];
+            const float inv_u = 1.f / sig_u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float dS[16];
+                tmem_ld16(tmem + TM_S + lane_off + 64 * half + 16 * q, dS);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) S[16 * q + e] = gam * S[16 * q + e] + dS[e] * inv_u;
+            }
+            const float sig_s_old = sig_s;
+            sig_s = row_scale(smax(), 0);
+            const bool more = k + 1 < nchunks;
+            if (more) store_state_f16(sig_s);
+            if (!mbar_wait(bar_q, k & 1, kWaitBudget)) *abort_c = 1;
+            if (!mbar_wait(bar_o, k & 1, kWaitBudget)) *abort_c = 1;
+            tc_fence_after();
+            uint32_t opk[16];  // outputs for t in [32 half, 32 half + 32), bf16 pairs
+            {
+                const float fq = 1.f / sig_s_old, fo = stsc[SC_PO] * inv_u;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float qa[16], oa[16];
+                    tmem_ld16(tmem + TM_Q + lane_off + 32 * half + 16 * q, qa);
+                    tmem_ld16(tmem + TM_X2 + lane_off + 32 * half + 16 * q, oa);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int t0 = 32 * half + 16 * q + 2 * c;
+                        const float o0 = stsc[SC_E + t0] * qa[2 * c] * fq + oa[2 * c] * fo;
+                        const float o1 = stsc[SC_E + t0 + 1] * qa[2 * c + 1] * fq + oa[2 * c + 1] * fo;
+                        opk[8 * q + c] = bf2_bits(__floats2bfloat162_rn(o0, o1));
+                    }
+                }
+            }
+            const int L = reinterpret_cast<const int *>(stsc)[SC_L];
+            tmem_wait_st();
+            tc_fence_before();
+            bar_sync(2, kWG);
+            if (*abort_c) break;
+            if (issuer) {
+                mbar_arrive(bar_empty + (k & 1));  // every MMA of block k has completed, scalars read
+                if (more) {
+                    if (!mbar_wait(bar_full + ((k + 1) & 1), ((k + 1) >> 1) & 1, kWaitBudget)) *abort_c = 1;
+                    tc_fence_after();
+                    issue_x1(k + 1);
+                    issue_x2q(k + 1);
+                }
+            }
+            // outputs of block k (off the state's critical path)
+            __nv_bfloat16 *ob = p.out + (c0 * p.Hv + h) * (long)DV + i;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int t = 32 * half + 2 * c;
+                if (t < L) ob[(long)t * p.Hv * DV] = __ushort_as_bfloat16((unsigned short)(opk[c] & 0xffffu));
+                if (t + 1 < L) ob[(long)(t + 1) * p.Hv * DV] = __ushort_as_bfloat16((unsigned short)(opk[c] >> 16));
+            }
+        }
+        if (*abort_c || *abort_p) {
+            if (tid == kWG) flag_error(p.status);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; j += 4)
+                *reinterpret_cast<float4 *>(p.state_out + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
     }
     tc_fence_before();
     __syncthreads();

@@ -105,8 +105,10 @@ def test_split_call_equals_one_call():
     gdn.gdn_prefill(d.q[cut:].contiguous(), d.k[cut:].contiguous(), d.v[cut:].contiguous(),
                     d.g[cut:].contiguous(), d.b[cut:].contiguous(), mid, s2, o2, B=1, chunk=64)
     torch.cuda.synchronize()
+    assert gdn.gdn_get_device_status() == gdn.GDN_OK
     assert_outputs_close(torch.cat([o1, o2]), out, 1e-2)
-    assert (s2 - so).norm() <= 1e-4 * so.norm()
+    # each route is within the oracle's state bar, so they are within twice it of each other
+    assert (s2 - so).norm() <= 2 * STATE_TOL * so.norm()
     check(b, torch.cat([o1, o2]), s2)
 
 

@@ -17,8 +17,8 @@
 //   T  = (I + A)^-1,  Tb = T diag(beta),  Tw = T diag(beta e)
 //   W  = Tw Kh                           (C x dk)
 //   U^T = V^T Tb^T - S W^T               (dv x C)      <- first state-dependent product
-//   S  <- gamma S + U^T diag(d) Kh       (dv x dk)     <- second state-dependent product
-//   O^T = S Qh^T diag(e) + U^T P^T       (dv x C)
+//   S  <- gamma S + U^T Kt,  Kt = diag(d) Kh           <- second state-dependent product
+//   O^T = S Qt^T + U^T P^T,  Qt = diag(e) Qh           (dv x C)
 // The state product is transposed so that the 128 state rows sit on the 128 TMEM
 // lanes: one thread owns one row of S in fp32 registers for the whole sequence,
 // and an fp16 copy of S is the A operand of the MMAs straight from TMEM.
@@ -72,11 +72,12 @@ constexpr uint32_t STAGE = 82944;
 // stage scalars (float index)
 constexpr int SC_D = 0, SC_E = 64, SC_GAMMA = 128, SC_X1 = 129, SC_X2 = 130, SC_PO = 131, SC_L = 132;
 // prep-private
-constexpr uint32_t RAW = 2 * STAGE;   // 48 KiB raw bf16 tiles: K (0, 8K), Q (16K, 24K), V (32K, 40K)
+constexpr uint32_t RAW = 2 * STAGE;   // 48 KiB raw bf16 tiles: [kb][K rows 0..63 | Q rows 64..127] (32K), V (32K, 40K)
 constexpr uint32_t TW = RAW + 49152;  //  8 KiB [t][s] fp16, scaled Tw; solve scratch X before
 constexpr uint32_t PSC = TW + 8192;   // prep scalars (float index below)
 constexpr int PS_G = 0, PS_BETA = 64, PS_AA = 128, PS_BB = 192, PS_EE = 256, PS_BE = 320, PS_DD = 384,
-              PS_SS = 448 /* [2][128] */, PS_FACT = 704, PS_RED = 712 /* [sites][8 warps][4] */;
+              PS_SS = 448 /* [2][128] */, PS_FACT = 704, PS_GMIN = 705, PS_GMAX = 706, PS_RK = 712, PS_RQ = 776,
+              PS_RKB = 840, PS_RED = 904 /* [sites][8 warps][4] */;
 constexpr int RED_V = 0, RED_TP = 1, RED_W = 2;  // reduction sites
 constexpr uint32_t CSC = PSC + 4 * (PS_RED + 3 * 32);  // chain scratch: [2 sites][2 halves][128] floats
 constexpr uint32_t BAR = CSC + 4 * 512;
@@ -91,15 +92,14 @@ constexpr uint32_t TM_X2 = 128;   // chain: S (-W)^T, then U^T P^T (64)
 constexpr uint32_t TM_Q = 192;    // chain: S Qh^T                 (64)
 constexpr uint32_t TM_S = 256;    // chain: U~^T Kh                (128)
 constexpr uint32_t TM_AS = 384;   // chain: fp16 S, A operand      (64 = 128 fp16)
-constexpr uint32_t TM_AUT = 448;  // chain: fp16 U^T diag(d)       (32)
-constexpr uint32_t TM_AU = 480;   // chain: fp16 U^T               (32)
+constexpr uint32_t TM_AU = 448;   // chain: fp16 U^T               (32)
 
 // instruction descriptor, kind::f16 with fp16 operands and an fp32 accumulator
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
     return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t ID_GRAM = idesc_f16(128, 64, 0, 0);
+constexpr uint32_t ID_GRAM_BF16 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_W = idesc_f16(128, 64, 1, 0);
 constexpr uint32_t ID_X1 = idesc_f16(128, 64, 1, 0);
 constexpr uint32_t ID_X2 = idesc_f16(128, 64, 0, 1);
@@ -144,6 +144,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
 }
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
@@ -181,14 +189,13 @@ __device__ __forceinline__ int sw(int t, int s) { return t * 64 + (s ^ ((t & 7) 
 __device__ void solve_unit_lower(const float *sA, float *sT, float *sX, int p, int bar_id) {
     if (p < 64) {
         const int b = p >> 4, c = p & 15;
-        float x[16];
+        float x[16];  // column c of the block inverse, right-looking: independent updates per step
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = (r == c) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc -= sA[sw(16 * b + r, 16 * b + s)] * x[s];
-            x[r] = acc;
-        }
+        for (int s = 0; s < 15; ++s)
+#pragma unroll
+            for (int r = s + 1; r < 16; ++r) x[r] -= sA[sw(16 * b + r, 16 * b + s)] * x[s];
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[sw(16 * b + r, 16 * b + c)] = x[r];
         for (int i = 0; i < b; ++i)
@@ -196,29 +203,43 @@ __device__ void solve_unit_lower(const float *sA, float *sT, float *sX, int p, i
             for (int r = 0; r < 16; ++r) sT[sw(16 * i + r, 16 * b + c)] = 0.f;
     }
     bar_sync(bar_id, kWG);
-    for (int d = 1; d < 4; ++d) {
-        const bool act = p < (4 - d) * 64;
-        const int blk = p >> 6, r = (p >> 2) & 15, c0 = (p & 3) * 4;
-        const int i = d + blk, j = blk;
-        if (act) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int k = j; k < i; ++k) {
+    // Level d (blocks i = j + d): X_ij = sum_{k=j}^{i-1} A_ik T_kj, T_ij = -T_ii X_ij.
+    // The X phase gives each (block, term k) its own 64 threads (4 adjacent outputs each), so
+    // 192..256 threads work in every phase; the T phase adds the d partial products.
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float a = sA[sw(16 * i + r, 16 * k + m)];
-                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + sw(16 * k + m, 16 * j + c0));
-                    acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
-                }
+    for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d;                   // blocks in this level
+        const int slot = p >> 6;                // (block, term) pair handled by this thread
+        const bool act = slot < nb * d;
+        const int blk = slot / d, kk = slot % d;
+        const int r = (p >> 2) & 15, c0 = (p & 3) * 4;
+        if (act) {
+            const int i = d + blk, j = blk, k = j + kk;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+                const float a = sA[sw(16 * i + r, 16 * k + m)], a2 = sA[sw(16 * i + r, 16 * k + m + 1)];
+                const float4 t4 = *reinterpret_cast<const float4 *>(sT + sw(16 * k + m, 16 * j + c0));
+                const float4 u4 = *reinterpret_cast<const float4 *>(sT + sw(16 * k + m + 1, 16 * j + c0));
+                acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                acc2.x += a2 * u4.x; acc2.y += a2 * u4.y; acc2.z += a2 * u4.z; acc2.w += a2 * u4.w;
             }
-            *reinterpret_cast<float4 *>(sX + blk * 256 + r * 16 + c0) = acc;
+            *reinterpret_cast<float4 *>(sX + slot * 256 + r * 16 + c0) =
+                make_float4(acc.x + acc2.x, acc.y + acc2.y, acc.z + acc2.z, acc.w + acc2.w);
         }
         bar_sync(bar_id, kWG);
-        if (act) {
+        if (p < nb * 64) {
+            const int tb = p >> 6, i = d + tb, j = tb;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const float a = sT[sw(16 * i + r, 16 * i + m)];
-                const float4 x4 = *reinterpret_cast<const float4 *>(sX + blk * 256 + m * 16 + c0);
+                float4 x4 = *reinterpret_cast<const float4 *>(sX + (tb * d) * 256 + m * 16 + c0);
+#pragma unroll
+                for (int q = 1; q < d; ++q) {
+                    const float4 y4 = *reinterpret_cast<const float4 *>(sX + (tb * d + q) * 256 + m * 16 + c0);
+                    x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
+                }
                 acc.x += a * x4.x; acc.y += a * x4.y; acc.z += a * x4.z; acc.w += a * x4.w;
             }
             *reinterpret_cast<float4 *>(sT + sw(16 * i + r, 16 * j + c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
@@ -283,8 +304,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_expect_tx(bar_tma, 6 * 8192);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-                tma_load_3d(sm + RAW + kb * 8192, &tm_k, kb * 64, hk, c_tok, bar_tma);
-                tma_load_3d(sm + RAW + 16384 + kb * 8192, &tm_q, kb * 64, hk, c_tok, bar_tma);
+                tma_load_3d(sm + RAW + kb * 16384, &tm_k, kb * 64, hk, c_tok, bar_tma);
+                tma_load_3d(sm + RAW + kb * 16384 + 8192, &tm_q, kb * 64, hk, c_tok, bar_tma);
                 tma_load_3d(sm + RAW + 32768 + kb * 8192, &tm_v, kb * 64, h, c_tok, bar_tma);
             }
         };
@@ -319,16 +340,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
             if (!mbar_wait(bar_tma, k & 1, kWaitBudget)) *abort_p = 1;
+            if (pt == 0) {  // Gram [K; Q] K^T on the raw bf16 tiles (exact products), overlapping the norms
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t d = desc_sw128(sb + RAW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                    mma_bf16(tmem + TM_GW, d, d, ID_GRAM_BF16, ks > 0);
+                }
+                mma_commit(bar_prep);
+            }
             bar_sync(1, kWG);
             if (*abort_p) break;
             // ---- row norms (half a row per thread), V maximum; warp 0 also scans the gates ----
             const int row = r & 63;  // K rows for r < 64, Q rows for r >= 64
-            const uint32_t raw_row = RAW + (r >= 64 ? 16384u : 0u) + half * 8192;
+            const uint32_t raw_row = RAW + half * 16384;  // stacked row r of K-block `half`
             uint4 raw8[8];
             float ssq = 0.f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                raw8[c] = *reinterpret_cast<const uint4 *>(sm + raw_row + swz(row, c));
+                raw8[c] = *reinterpret_cast<const uint4 *>(sm + raw_row + swz(r, c));
                 float x[8];
                 unpack8(raw8[c], x);
 #pragma unroll
@@ -360,6 +390,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 x1 += __shfl_sync(0xffffffffu, x0, 31);
                 ps[PS_G + lane] = x0;
                 ps[PS_G + lane + 32] = x1;
+                float mn = fminf(x0, x1), mx = fmaxf(x0, x1);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                }
+                if (lane == 0) {
+                    ps[PS_GMIN] = mn;
+                    ps[PS_GMAX] = mx;
+                }
             }
             bar_sync(1, kWG);
             const float GL = ps[PS_G + L - 1];
@@ -368,16 +408,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int w = 0; w < 8; ++w) vm = fmaxf(vm, red[RED_V * 32 + w * 4]);
             const float sig_v = pow2_scale(vm);
+            if (half == 0) (r < 64 ? ps + PS_RK : ps + PS_RQ)[row] = rnorm;
+            const float qscale = r < 64 ? rnorm : rnorm * expf(ps[PS_G + row]);  // Kh rows; Qt = e rq Q rows
             if (pt < C) {  // per-token exp factors, computed once
-                float gmin = ps[PS_G], gmax = ps[PS_G];
-#pragma unroll 8
-                for (int t = 1; t < C; ++t) {
-                    gmin = fminf(gmin, ps[PS_G + t]);
-                    gmax = fmaxf(gmax, ps[PS_G + t]);
-                }
+                const float gmin = ps[PS_GMIN], gmax = ps[PS_GMAX];
                 const float G = ps[PS_G + pt];
                 ps[PS_AA + pt] = expf(G - gmin);
                 ps[PS_BB + pt] = expf(gmin - G);
+                ps[PS_RKB + pt] = expf(gmin - G) * (pt < L ? rsqrtf(ps[PS_SS + pt] + ps[PS_SS + 128 + pt] + kNormEps) : 0.f);
                 const float e = expf(G);
                 ps[PS_EE + pt] = e;
                 ps[PS_BE + pt] = ps[PS_BETA + pt] * e;
@@ -390,7 +428,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int c = 0; c < 8; ++c) {
                 float x[8];
                 unpack8(raw8[c], x);
-                *reinterpret_cast<uint4 *>(st + ST_KQ + half * 16384 + swz(r, c)) = pack8_f16(x, rnorm);
+                *reinterpret_cast<uint4 *>(st + ST_KQ + half * 16384 + swz(r, c)) = pack8_f16(x, qscale);
             }
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -404,19 +442,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             bar_sync(1, kWG);
             if (*abort_p) break;
-            if (pt == 0) {
-                if (k + 1 < nchunks) issue_tma((int)(c0 + C));  // raw tiles consumed: fetch the next block
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {  // Gram [Kh; Qh] Kh^T
-                    const uint64_t d = desc_sw128(stb + ST_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                    mma_f16_ss(tmem + TM_GW, d, d, ID_GRAM, ks > 0);
-                }
-                mma_commit(bar_prep);
-            }
-            if (!mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;
+            if (!mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;  // Gram done: raw tiles free
             ph_prep ^= 1;
             tc_fence_after();
+            if (pt == 0 && k + 1 < nchunks) issue_tma((int)(c0 + C));  // fetch the next block's tiles
             // ---- A rows (fp32, swizzled, for the solve); P rows stay in registers ----
             const bool factor = ps[PS_FACT] != 0.f;
             float pv[32];
@@ -426,15 +455,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_ld16(tmem + TM_GW + lane_off + 32 * half, v0);
                 tmem_ld16(tmem + TM_GW + lane_off + 32 * half + 16, v1);
                 const float at = ps[PS_AA + row], Gt = ps[PS_G + row];
-                const float bt = r < 64 ? ps[PS_BETA + row] * at : at;
+                const float nt = r < 64 ? ps[PS_RK + row] * ps[PS_BETA + row] : ps[PS_RQ + row];
+                const float bt = nt * at;
                 if (factor) {  // uniform branch: e^{G_t-G_s} = a_t b_s
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) pv[e] = (e < 16 ? v0[e] : v1[e - 16]) * bt * ps[PS_BB + 32 * half + e];
+                    for (int e = 0; e < 32; ++e)
+                        pv[e] = (e < 16 ? v0[e] : v1[e - 16]) * bt * ps[PS_RKB + 32 * half + e];
                 } else {
-                    const float bb = r < 64 ? ps[PS_BETA + row] : 1.f;
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        pv[e] = (e < 16 ? v0[e] : v1[e - 16]) * bb * expf(Gt - ps[PS_G + 32 * half + e]);
+                        pv[e] = (e < 16 ? v0[e] : v1[e - 16]) * nt * ps[PS_RK + 32 * half + e] *
+                                expf(Gt - ps[PS_G + 32 * half + e]);
                 }
                 if (r < 64) {
 #pragma unroll
@@ -538,6 +569,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     *reinterpret_cast<uint4 *>(st + ST_W + swz(r, 4 * half + cc)) = pack8_f16(&w0[8 * cc], f);
                     *reinterpret_cast<uint4 *>(st + ST_W + swz(r, 4 * half + 2 + cc)) = pack8_f16(&w1[8 * cc], f);
                 }
+                {  // thread (row r < 64 of Kh, K-block half): scale by d_r in place
+                    const int kr = r & 63, kh = (r >> 6) + 2 * half;  // 64 rows x 4 chunk groups
+                    const float dr = ps[PS_DD + kr];
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int kb = kh >> 1, c = (kh & 1) * 4 + 2 * c2;
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            uint4 *pk = reinterpret_cast<uint4 *>(st + ST_KQ + kb * 16384 + swz(kr, c + cc));
+                            uint4 v = *pk;
+                            __half2 *hv = reinterpret_cast<__half2 *>(&v);
+                            const __half2 d2 = __float2half2_rn(dr);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) hv[e] = __hmul2(hv[e], d2);
+                            *pk = v;
+                        }
+                    }
+                }
                 if (pt < C) {
                     stsc[SC_D + pt] = ps[PS_DD + pt];
                     stsc[SC_E + pt] = ps[PS_EE + pt];
@@ -593,18 +642,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_st8(tmem + TM_AS + lane_off + 32 * half + 8 * c8, rr);
             }
         };
-        auto issue_x2q = [&](int k) {  // S(-W)^T and S Qh^T for block k
+        auto issue_x2 = [&](int k) {  // S(-W)^T for block k: the state's critical product
             const uint32_t stb = sb + (k & 1) * STAGE;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 mma_f16_ts(tmem + TM_X2, tmem + TM_AS + 8 * ks, desc_sw128(stb + ST_W + ks * 2048, 8192, 1024), ID_X2,
                            ks > 0);
             mma_commit(bar_x);
+        };
+        auto issue_q = [&](int k) {  // S Qt^T for block k (outputs only)
+            const uint32_t stb = sb + (k & 1) * STAGE;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 mma_f16_ts(tmem + TM_Q, tmem + TM_AS + 8 * ks,
                            desc_sw128(stb + ST_KQ + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024), ID_Q, ks > 0);
-            mma_commit(bar_q);
         };
         auto issue_x1 = [&](int k) {  // V^T Tb^T for block k (state independent)
             const uint32_t stb = sb + (k & 1) * STAGE;
@@ -615,6 +666,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         };
 
         float sig_s = row_scale(smax(), 0);
+        bool x1_next = false;  // issuer only: the next block's V^T Tb^T is already issued
         if (nchunks > 0) {
             if (!mbar_wait(bar_full + 0, 0, kWaitBudget)) *abort_c = 1;
             store_state_f16(sig_s);
@@ -624,7 +676,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (issuer && !*abort_c) {
                 tc_fence_after();
                 issue_x1(0);
-                issue_x2q(0);
+                issue_x2(0);
             }
         }
         for (int k = 0; k < nchunks && !*abort_c; ++k) {
@@ -635,32 +687,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!mbar_wait(bar_x, k & 1, kWaitBudget)) *abort_c = 1;
             tc_fence_after();
             const float f1 = stsc[SC_X1], f2 = stsc[SC_X2] / sig_s;
+            float u[32];  // U^T[i][t], t in [32 half, 32 half + 32)
             float m = 0.f;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                float a[16], bx[16];
-                tmem_ld16(tmem + TM_X1 + lane_off + 32 * half + 16 * q, a);
-                tmem_ld16(tmem + TM_X2 + lane_off + 32 * half + 16 * q, bx);
+                uint32_t a[16], bx[16];
+                tmem_ld16_nw(tmem + TM_X1 + lane_off + 32 * half + 16 * q, a);
+                tmem_ld16_nw(tmem + TM_X2 + lane_off + 32 * half + 16 * q, bx);
+                tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    m = fmaxf(m, fabsf(a[e] * f1 + bx[e] * f2) * fmaxf(1.f, stsc[SC_D + 32 * half + 16 * q + e]));
+                for (int e = 0; e < 16; ++e) {
+                    const float uv = __uint_as_float(a[e]) * f1 + __uint_as_float(bx[e]) * f2;
+                    u[16 * q + e] = uv;
+                    m = fmaxf(m, fabsf(uv));
+                }
             }
             const float sig_u = row_scale(m, 1);
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                float a[16], bx[16];
-                tmem_ld16(tmem + TM_X1 + lane_off + 32 * half + 16 * q, a);
-                tmem_ld16(tmem + TM_X2 + lane_off + 32 * half + 16 * q, bx);
-                uint32_t rd[8], ru[8];
+                uint32_t ru[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int t0 = 32 * half + 16 * q + 2 * c;
-                    const float u0 = sig_u * (a[2 * c] * f1 + bx[2 * c] * f2);
-                    const float u1 = sig_u * (a[2 * c + 1] * f1 + bx[2 * c + 1] * f2);
-                    rd[c] = h2_bits(u0 * stsc[SC_D + t0], u1 * stsc[SC_D + t0 + 1]);
-                    ru[c] = h2_bits(u0, u1);
-                }
-                tmem_st8(tmem + TM_AUT + lane_off + 16 * half + 8 * q, rd);
+                for (int c = 0; c < 8; ++c) ru[c] = h2_bits(sig_u * u[16 * q + 2 * c], sig_u * u[16 * q + 2 * c + 1]);
                 tmem_st8(tmem + TM_AU + lane_off + 16 * half + 8 * q, ru);
             }
             tmem_wait_st();
@@ -671,15 +718,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
                 const uint32_t stb = sb + (k & 1) * STAGE;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)  // U~^T Kh  (B = Kh rows, MN-major)
-                    mma_f16_ts(tmem + TM_S, tmem + TM_AUT + 8 * ks, desc_sw128(stb + ST_KQ + ks * 2048, 16384, 1024),
+                for (int ks = 0; ks < 4; ++ks)  // U^T Kt  (B = diag(d) Kh rows, MN-major)
+                    mma_f16_ts(tmem + TM_S, tmem + TM_AU + 8 * ks, desc_sw128(stb + ST_KQ + ks * 2048, 16384, 1024),
                                ID_S, ks > 0);
                 mma_commit(bar_s);
+                issue_q(k);  // outputs: behind the state update in the tensor pipe
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)  // U^T P^T
                     mma_f16_ts(tmem + TM_X2, tmem + TM_AU + 8 * ks, desc_sw128(stb + ST_P + ks * 32, 16, 1024), ID_O,
                                ks > 0);
-                mma_commit(bar_o);
+                mma_commit(bar_o);  // covers Q and O
+                // the next block's state-independent V^T Tb^T, now if its operands are already there
+                // (TM_X1 was read in E1); otherwise just before the next S(-W)^T
+                x1_next = false;
+                if (k + 1 < nchunks && mbar_try_wait(bar_full + ((k + 1) & 1), ((k + 1) >> 1) & 1)) {
+                    issue_x1(k + 1);
+                    x1_next = true;
+                }
             }
             // ---- E2: state update (columns j of this half), next A operand, outputs ----
             if (!mbar_wait(bar_s, k & 1, kWaitBudget)) *abort_c = 1;
@@ -687,32 +742,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float gam = stsc[SC_GAMMA];
             const float inv_u = 1.f / sig_u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float dS[16];
-                tmem_ld16(tmem + TM_S + lane_off + 64 * half + 16 * q, dS);
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t d0[16], d1[16];
+                tmem_ld16_nw(tmem + TM_S + lane_off + 64 * half + 32 * q2, d0);
+                tmem_ld16_nw(tmem + TM_S + lane_off + 64 * half + 32 * q2 + 16, d1);
+                tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) S[16 * q + e] = gam * S[16 * q + e] + dS[e] * inv_u;
+                for (int e = 0; e < 16; ++e) {
+                    S[32 * q2 + e] = gam * S[32 * q2 + e] + __uint_as_float(d0[e]) * inv_u;
+                    S[32 * q2 + 16 + e] = gam * S[32 * q2 + 16 + e] + __uint_as_float(d1[e]) * inv_u;
+                }
             }
             const float sig_s_old = sig_s;
             sig_s = row_scale(smax(), 0);
             const bool more = k + 1 < nchunks;
-            if (more) store_state_f16(sig_s);
-            if (!mbar_wait(bar_q, k & 1, kWaitBudget)) *abort_c = 1;
-            if (!mbar_wait(bar_o, k & 1, kWaitBudget)) *abort_c = 1;
+            if (!mbar_wait(bar_o, k & 1, kWaitBudget)) *abort_c = 1;  // Q and O of block k: A_S is free
             tc_fence_after();
+            if (more) store_state_f16(sig_s);
             uint32_t opk[16];  // outputs for t in [32 half, 32 half + 32), bf16 pairs
             {
                 const float fq = 1.f / sig_s_old, fo = stsc[SC_PO] * inv_u;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    float qa[16], oa[16];
-                    tmem_ld16(tmem + TM_Q + lane_off + 32 * half + 16 * q, qa);
-                    tmem_ld16(tmem + TM_X2 + lane_off + 32 * half + 16 * q, oa);
+                    uint32_t qa[16], oa[16];
+                    tmem_ld16_nw(tmem + TM_Q + lane_off + 32 * half + 16 * q, qa);
+                    tmem_ld16_nw(tmem + TM_X2 + lane_off + 32 * half + 16 * q, oa);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const int t0 = 32 * half + 16 * q + 2 * c;
-                        const float o0 = stsc[SC_E + t0] * qa[2 * c] * fq + oa[2 * c] * fo;
-                        const float o1 = stsc[SC_E + t0 + 1] * qa[2 * c + 1] * fq + oa[2 * c + 1] * fo;
+                        const float o0 = __uint_as_float(qa[2 * c]) * fq + __uint_as_float(oa[2 * c]) * fo;
+                        const float o1 = __uint_as_float(qa[2 * c + 1]) * fq + __uint_as_float(oa[2 * c + 1]) * fo;
                         opk[8 * q + c] = bf2_bits(__floats2bfloat162_rn(o0, o1));
                     }
                 }
@@ -725,10 +784,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (issuer) {
                 mbar_arrive(bar_empty + (k & 1));  // every MMA of block k has completed, scalars read
                 if (more) {
-                    if (!mbar_wait(bar_full + ((k + 1) & 1), ((k + 1) >> 1) & 1, kWaitBudget)) *abort_c = 1;
+                    if (!x1_next) {
+                        if (!mbar_wait(bar_full + ((k + 1) & 1), ((k + 1) >> 1) & 1, kWaitBudget)) *abort_c = 1;
+                        tc_fence_after();
+                        issue_x1(k + 1);
+                    }
                     tc_fence_after();
-                    issue_x1(k + 1);
-                    issue_x2q(k + 1);
+                    issue_x2(k + 1);
                 }
             }
             // outputs of block k (off the state's critical path)

@@ -46,7 +46,7 @@ PREFILL_FLOPS_PER_TOKEN = HV * (5 * 2 * CHUNK * DK + 3 * 2 * DK * DV)  # chunk G
 DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + IO_BYTES_PER_TOKEN
 # DRAM bytes per launch from the committed ncu captures (profiles/); None once a kernel
 # has changed since its capture.
-TRAFFIC = {"prefill": None, "decode": 480.2e6}
+TRAFFIC = {"prefill": 75.67e6, "decode": 480.2e6}
 
 
 def peaks():
@@ -74,7 +74,7 @@ class Clocks:
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -292,7 +292,7 @@ def cpu_baseline_sample(threads=None, tokens=T_PREFILL, steps=1, warmup=0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -339,7 +339,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     b_nx = to_f32(p.b[cn * p.Hv + h]);
                 }
             }
-            if (!mbar_wait(bar_tma, k & 1, kWaitBudget)) *abort_p = 1;
+            if (!mbar_wait(bar_tma, k & 1, kWaitBudget)) *abort_p = 1;  // every reader of the tiles waits (asleep)
             if (pt == 0) {  // Gram [K; Q] K^T on the raw bf16 tiles (exact products), overlapping the norms
                 tc_fence_after();
 #pragma unroll
@@ -423,7 +423,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (pt == 0) ps[PS_FACT] = (gmax - gmin) < 80.f ? 1.f : 0.f;  // a_t b_s = e^{G_t-G_s} safely
             }
             // ---- wait until the chain released this stage (block k-2), then write fp16 operands ----
-            if (k >= 2 && !mbar_wait(bar_empty + s, ((k - 2) >> 1) & 1, kWaitBudget)) *abort_p = 1;
+            if (k >= 2) {
+                if (pt == 0 && !mbar_wait(bar_empty + s, ((k - 2) >> 1) & 1, kWaitBudget)) *abort_p = 1;
+                bar_sync(1, kWG);
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 float x[8];
@@ -442,8 +445,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             bar_sync(1, kWG);
             if (*abort_p) break;
-            if (!mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;  // Gram done: raw tiles free
+            if (pt == 0 && !mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;  // Gram done: raw tiles free
             ph_prep ^= 1;
+            bar_sync(1, kWG);
             tc_fence_after();
             if (pt == 0 && k + 1 < nchunks) issue_tma((int)(c0 + C));  // fetch the next block's tiles
             // ---- A rows (fp32, swizzled, for the solve); P rows stay in registers ----
@@ -545,8 +549,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                desc_sw128(sb + TW + ks * 32, 16, 1024), ID_W, ks > 0);
                 mma_commit(bar_prep);
             }
-            if (!mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;
+            if (pt == 0 && !mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;
             ph_prep ^= 1;
+            bar_sync(1, kWG);
             tc_fence_after();
             {  // thread (j = r, half): W^T row j over t in this half -> MN-major row j of the -W operand
                 float w0[16], w1[16];
@@ -622,6 +627,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int j = 0; j < 64; ++j) S[j] = 0.f;
         }
         // per-row power-of-two scale: both halves' maxima through shared memory
+        // one thread polls the mbarrier (sleeping), the other 255 wait on the group barrier
+        auto group_wait = [&](uint64_t *bar, uint32_t phase) {
+            if (issuer && !mbar_wait(bar, phase, kWaitBudget)) *abort_c = 1;
+            bar_sync(2, kWG);
+        };
         auto row_scale = [&](float m, int site) {
             cx[site * 256 + half * 128 + i] = m;
             bar_sync(2, kWG);
@@ -668,7 +678,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float sig_s = row_scale(smax(), 0);
         bool x1_next = false;  // issuer only: the next block's V^T Tb^T is already issued
         if (nchunks > 0) {
-            if (!mbar_wait(bar_full + 0, 0, kWaitBudget)) *abort_c = 1;
+            group_wait(bar_full + 0, 0);
             store_state_f16(sig_s);
             tmem_wait_st();
             tc_fence_before();
@@ -682,9 +692,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int k = 0; k < nchunks && !*abort_c; ++k) {
             const long c0 = bos + (long)k * C;
             const float *stsc = reinterpret_cast<const float *>(sm + (k & 1) * STAGE + ST_SC);
-            if (!mbar_wait(bar_full + (k & 1), (k >> 1) & 1, kWaitBudget)) *abort_c = 1;  // scalars of block k
+            group_wait(bar_full + (k & 1), (k >> 1) & 1);  // scalars of block k
             // ---- E1: U^T = X1 / (sig_v sig_b) + X2 / (sig_s sig_ww) -> fp16 U~^T, U^T (columns t of this half) ----
-            if (!mbar_wait(bar_x, k & 1, kWaitBudget)) *abort_c = 1;
+            group_wait(bar_x, k & 1);
             tc_fence_after();
             const float f1 = stsc[SC_X1], f2 = stsc[SC_X2] / sig_s;
             float u[32];  // U^T[i][t], t in [32 half, 32 half + 32)
@@ -737,7 +747,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
             // ---- E2: state update (columns j of this half), next A operand, outputs ----
-            if (!mbar_wait(bar_s, k & 1, kWaitBudget)) *abort_c = 1;
+            group_wait(bar_s, k & 1);
             tc_fence_after();
             const float gam = stsc[SC_GAMMA];
             const float inv_u = 1.f / sig_u;
@@ -756,7 +766,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float sig_s_old = sig_s;
             sig_s = row_scale(smax(), 0);
             const bool more = k + 1 < nchunks;
-            if (!mbar_wait(bar_o, k & 1, kWaitBudget)) *abort_c = 1;  // Q and O of block k: A_S is free
+            group_wait(bar_o, k & 1);  // Q and O of block k: A_S is free
             tc_fence_after();
             if (more) store_state_f16(sig_s);
             uint32_t opk[16];  // outputs for t in [32 half, 32 half + 32), bf16 pairs

@@ -45,11 +45,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
         : "memory");
     return ok != 0;
 }
+// try_wait that lets the hardware suspend the thread (up to ~ns_hint) instead of spinning
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t phase, uint32_t ns_hint) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(phase), "r"(ns_hint)
+        : "memory");
+    return ok != 0;
+}
 // Wait for `phase` to complete; give up after `budget` SM cycles and return false.
+// The thread sleeps inside try_wait between checks, so waiting warps do not take issue slots.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase, long long budget) {
     if (mbar_try_wait(bar, phase)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, phase))
+    while (!mbar_try_wait_sleep(bar, phase, 20000u))
         if (clock64() - t0 > budget) return false;
     return true;
 }

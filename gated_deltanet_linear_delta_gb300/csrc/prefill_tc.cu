@@ -42,6 +42,8 @@
 // Rows t >= L of a partial block get zero kh, qh, beta, d, so they contribute
 // nothing; their outputs are not stored.
 #include <cuda.h>
+#include <cstdio>
+#include <cstdlib>
 #include <cuda_fp16.h>
 
 #include "gdn_common.cuh"
@@ -116,10 +118,23 @@ struct TcParams {
     int B, Hk, Hv;
     long T, Ttot;
     int *status;
+    int P;  // CTAs per value head (a thread-block cluster); rank 0 carries the state
+    int F;  // first rank that prepares blocks: block k is prepared by rank F + k % (P - F)
 };
 
 // ---- small helpers ----
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// barrier that also returns, to every participant, whether any of them passed `pred` true:
+// a give-up decision that all threads of a group take together
+__device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -257,14 +272,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t sb = smem_u32(sm);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
     uint64_t *bar_tma = bars + 0, *bar_prep = bars + 1, *bar_full = bars + 2, *bar_empty = bars + 4;
-    uint64_t *bar_x = bars + 6, *bar_q = bars + 7, *bar_s = bars + 8, *bar_o = bars + 9;
+    uint64_t *bar_x = bars + 6, *bar_fin_p = bars + 7, *bar_s = bars + 8, *bar_o = bars + 9;
+    uint64_t *bar_fin_c = bars + 11;  // a group's last MMAs, waited for before leaving after a give-up
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
-    // one abort flag per warpgroup pair, written only by its own threads and read after its own barriers
-    volatile int *abort_p = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    volatile int *abort_c = abort_p + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int P = p.P, F = p.F, NP = P - F;
+    const int rank = P > 1 ? (int)cluster_ctarank() : 0;
+    const int h = blockIdx.x / P, n = blockIdx.y;
     const int hk = h / (p.Hv / p.Hk);
     long bos, eos;
     if (!seq_bounds(p.cu, n, p.B, p.cu ? p.Ttot : p.T, &bos, &eos, p.status)) return;
@@ -278,25 +293,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(bar_empty + s, 1);
         }
         mbar_init(bar_x, 1);
-        mbar_init(bar_q, 1);
+        mbar_init(bar_fin_p, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
+        mbar_init(bar_fin_c, 1);
         fence_mbar_init();
-        *abort_p = 0;
-        *abort_c = 0;
     }
     if (warp == 0) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
+    if (P > 1) cluster_sync();  // every CTA's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
     const int half = (tid >> 7) & 1;                              // which half of a row this thread owns
     const int r = tid & 127;                                      // TMEM lane = row
 
-    if (tid < kWG) {
+    if (tid < kWG && rank >= F) {
         // ======================= prep =======================
+        // This CTA prepares blocks first, first + NP, ...; rank 0 writes them straight into its
+        // stage k & 1, the other ranks into a local buffer (alternating two) that one bulk copy
+        // moves into rank 0's stage once the chain has released it.
         const int pt = tid;
+        const int first = rank - F;
+        const bool local = rank == 0;
+        uint32_t nwait[2] = {0u, 0u};  // completed waits on empty[0], empty[1]
+        // Every wait gives up after kWaitBudget cycles and sets `ab` in the waiting thread; the group
+        // leaves the loop together at the next bar_any. Tiles requested and not yet waited for are
+        // waited for (bounded) before the CTA may leave.
+        bool ab = false, failed = false;
+        int tma_issued = 0, tma_waited = 0;
         float *ps = reinterpret_cast<float *>(sm + PSC);
         float *red = ps + PS_RED;
         uint32_t ph_prep = 0;
@@ -309,23 +335,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tma_load_3d(sm + RAW + 32768 + kb * 8192, &tm_v, kb * 64, h, c_tok, bar_tma);
             }
         };
-        if (pt == 0 && nchunks > 0) {
+        if (pt == 0 && first < nchunks) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            issue_tma((int)bos);
+            issue_tma((int)(bos + (long)first * C));
+            tma_issued = 1;
         }
         float g_nx = 0.f, b_nx = 0.f;  // gates of the next block, fetched one block ahead
-        if (pt < C && nchunks > 0 && pt < eos - bos) {
-            g_nx = to_f32(p.g[(bos + pt) * p.Hv + h]);
-            b_nx = to_f32(p.b[(bos + pt) * p.Hv + h]);
+        if (pt < C && first < nchunks && bos + (long)first * C + pt < eos) {
+            g_nx = to_f32(p.g[(bos + (long)first * C + pt) * p.Hv + h]);
+            b_nx = to_f32(p.b[(bos + (long)first * C + pt) * p.Hv + h]);
         }
-        for (int k = 0; k < nchunks; ++k) {
+        int jb = 0;  // this CTA's job count
+        for (int k = first; k < nchunks; k += NP, ++jb) {
             const long c0 = bos + (long)k * C;
             const int L = (int)min((long)C, eos - c0);
-            const int s = k & 1;
-            uint8_t *st = sm + s * STAGE;
-            const uint32_t stb = sb + s * STAGE;
+            const int s = k & 1;               // rank 0's stage for block k
+            const int sl = local ? s : jb & 1;  // where this CTA builds it
+            uint8_t *st = sm + sl * STAGE;
+            const uint32_t stb = sb + sl * STAGE;
             float *stsc = reinterpret_cast<float *>(st + ST_SC);
             float *sA = reinterpret_cast<float *>(st + ST_W);
             float *sT = reinterpret_cast<float *>(st + ST_TB);
@@ -333,13 +362,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (pt < C) {
                 ps[PS_G + pt] = pt < L ? g_nx : 0.f;
                 ps[PS_BETA + pt] = pt < L ? sigmoidf_(b_nx) : 0.f;
-                const long cn = c0 + C + pt;
-                if (k + 1 < nchunks && cn < eos) {
+                const long cn = c0 + (long)NP * C + pt;
+                if (k + NP < nchunks && cn < eos) {
                     g_nx = to_f32(p.g[cn * p.Hv + h]);
                     b_nx = to_f32(p.b[cn * p.Hv + h]);
                 }
             }
-            if (!mbar_wait(bar_tma, k & 1, kWaitBudget)) *abort_p = 1;  // every reader of the tiles waits (asleep)
+            if (!mbar_wait(bar_tma, jb & 1, kWaitBudget)) ab = true;  // every reader of the tiles waits (asleep)
+            tma_waited = jb + 1;
             if (pt == 0) {  // Gram [K; Q] K^T on the raw bf16 tiles (exact products), overlapping the norms
                 tc_fence_after();
 #pragma unroll
@@ -349,8 +379,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 mma_commit(bar_prep);
             }
-            bar_sync(1, kWG);
-            if (*abort_p) break;
+            if (bar_any(1, kWG, ab)) { failed = true; break; }
             // ---- row norms (half a row per thread), V maximum; warp 0 also scans the gates ----
             const int row = r & 63;  // K rows for r < 64, Q rows for r >= 64
             const uint32_t raw_row = RAW + half * 16384;  // stacked row r of K-block `half`
@@ -422,10 +451,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ps[PS_DD + pt] = pt < L ? expf(GL - G) : 0.f;
                 if (pt == 0) ps[PS_FACT] = (gmax - gmin) < 80.f ? 1.f : 0.f;  // a_t b_s = e^{G_t-G_s} safely
             }
-            // ---- wait until the chain released this stage (block k-2), then write fp16 operands ----
-            if (k >= 2) {
-                if (pt == 0 && !mbar_wait(bar_empty + s, ((k - 2) >> 1) & 1, kWaitBudget)) *abort_p = 1;
-                bar_sync(1, kWG);
+            // ---- rank 0: wait until the chain released this stage (block k-2), then write fp16 operands ----
+            if (local && k >= 2) {
+                if (pt == 0 && !mbar_wait(bar_empty + s, nwait[s] & 1, kWaitBudget)) ab = true;
+                ++nwait[s];
+                if (bar_any(1, kWG, ab)) { failed = true; break; }
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -444,12 +474,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             fence_async_smem();
             tc_fence_before();
             bar_sync(1, kWG);
-            if (*abort_p) break;
-            if (pt == 0 && !mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;  // Gram done: raw tiles free
+            if (pt == 0 && !mbar_wait(bar_prep, ph_prep, kWaitBudget)) ab = true;  // Gram done: raw tiles free
             ph_prep ^= 1;
-            bar_sync(1, kWG);
+            if (bar_any(1, kWG, ab)) { failed = true; break; }
             tc_fence_after();
-            if (pt == 0 && k + 1 < nchunks) issue_tma((int)(c0 + C));  // fetch the next block's tiles
+            if (pt == 0 && k + NP < nchunks) {  // this CTA's next tiles
+                issue_tma((int)(c0 + (long)NP * C));
+                tma_issued = jb + 2;
+            }
             // ---- A rows (fp32, swizzled, for the solve); P rows stay in registers ----
             const bool factor = ps[PS_FACT] != 0.f;
             float pv[32];
@@ -549,9 +581,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                desc_sw128(sb + TW + ks * 32, 16, 1024), ID_W, ks > 0);
                 mma_commit(bar_prep);
             }
-            if (pt == 0 && !mbar_wait(bar_prep, ph_prep, kWaitBudget)) *abort_p = 1;
+            if (pt == 0 && !mbar_wait(bar_prep, ph_prep, kWaitBudget)) ab = true;
             ph_prep ^= 1;
-            bar_sync(1, kWG);
+            if (bar_any(1, kWG, ab)) { failed = true; break; }
             tc_fence_after();
             {  // thread (j = r, half): W^T row j over t in this half -> MN-major row j of the -W operand
                 float w0[16], w1[16];
@@ -607,9 +639,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             fence_async_smem();
             tc_fence_before();
             bar_sync(1, kWG);
-            if (pt == 0) mbar_arrive(bar_full + s);
+            if (local) {
+                if (pt == 0) mbar_arrive(bar_full + s);
+            } else if (pt == 0) {
+                // rank 0's stage s is free once the chain has finished block k-2. (This buffer was last
+                // copied out two jobs ago, block k - 2 NP; the previous job's wait, block k - NP - 2
+                // finished, already implied that copy had landed: NP >= 2 for every rank > 0.)
+                bool ok = true;
+                if (k >= 2) {
+                    ok = mbar_wait_cluster(bar_empty + s, nwait[s] & 1, kWaitBudget);
+                    ++nwait[s];
+                }
+                if (!ok) {
+                    ab = true;
+                } else {
+                    const uint32_t full_r = mapa_shared(smem_u32(bar_full + s), 0);
+                    const uint32_t dst_r = mapa_shared(sb + s * STAGE, 0);
+                    mbar_arrive_expect_tx_cluster(full_r, STAGE);
+#pragma unroll
+                    for (uint32_t off = 0; off < STAGE; off += 16384)
+                        bulk_copy_to_cluster(dst_r + off, st + off, min(16384u, STAGE - off), full_r);
+                }
+            }
+            if (!local && bar_any(1, kWG, ab)) { failed = true; break; }
         }
-    } else {
+        if (failed && pt == 0) {  // nothing of this group may still be in flight when the CTA leaves
+            for (int j = tma_waited; j < tma_issued; ++j) mbar_wait(bar_tma, j & 1, kWaitBudget);
+            mma_commit(bar_fin_p);
+            mbar_wait(bar_fin_p, 0, kWaitBudget);
+            flag_error(p.status);
+        }
+    } else if (tid >= kWG && rank == 0) {
         // ======================= chain =======================
         const int i = r;             // state row (TMEM lane)
         const bool issuer = (tid == kWG);
@@ -626,12 +686,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int j = 0; j < 64; ++j) S[j] = 0.f;
         }
-        // per-row power-of-two scale: both halves' maxima through shared memory
-        // one thread polls the mbarrier (sleeping), the other 255 wait on the group barrier
+        // One thread polls the mbarrier (sleeping), the other 255 wait on the group barrier. A wait
+        // that gives up sets `ab` in the issuer, which stops issuing; the group leaves the loop
+        // together at its next bar_any.
+        bool ab = false, failed = false;
         auto group_wait = [&](uint64_t *bar, uint32_t phase) {
-            if (issuer && !mbar_wait(bar, phase, kWaitBudget)) *abort_c = 1;
+            if (issuer && !ab && !mbar_wait(bar, phase, kWaitBudget)) ab = true;
             bar_sync(2, kWG);
         };
+        // per-row power-of-two scale: both halves' maxima through shared memory
         auto row_scale = [&](float m, int site) {
             cx[site * 256 + half * 128 + i] = m;
             bar_sync(2, kWG);
@@ -683,13 +746,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_wait_st();
             tc_fence_before();
             bar_sync(2, kWG);
-            if (issuer && !*abort_c) {
+            if (issuer && !ab) {
                 tc_fence_after();
                 issue_x1(0);
                 issue_x2(0);
             }
         }
-        for (int k = 0; k < nchunks && !*abort_c; ++k) {
+        for (int k = 0; k < nchunks; ++k) {
             const long c0 = bos + (long)k * C;
             const float *stsc = reinterpret_cast<const float *>(sm + (k & 1) * STAGE + ST_SC);
             group_wait(bar_full + (k & 1), (k >> 1) & 1);  // scalars of block k
@@ -722,8 +785,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             tmem_wait_st();
             tc_fence_before();
-            bar_sync(2, kWG);
-            if (*abort_c) break;
+            if (bar_any(2, kWG, ab)) { failed = true; break; }
             if (issuer) {
                 tc_fence_after();
                 const uint32_t stb = sb + (k & 1) * STAGE;
@@ -789,18 +851,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int L = reinterpret_cast<const int *>(stsc)[SC_L];
             tmem_wait_st();
             tc_fence_before();
-            bar_sync(2, kWG);
-            if (*abort_c) break;
+            if (bar_any(2, kWG, ab)) { failed = true; break; }
+            if (issuer && k + 2 < nchunks) {  // every MMA of block k has completed, scalars read:
+                const int to = F + (k + 2) % NP;  // release stage k & 1 to the producer of block k + 2
+                if (to == 0)
+                    mbar_arrive(bar_empty + (k & 1));
+                else
+                    mbar_arrive_cluster(mapa_shared(smem_u32(bar_empty + (k & 1)), (uint32_t)to));
+            }
             if (issuer) {
-                mbar_arrive(bar_empty + (k & 1));  // every MMA of block k has completed, scalars read
                 if (more) {
                     if (!x1_next) {
-                        if (!mbar_wait(bar_full + ((k + 1) & 1), ((k + 1) >> 1) & 1, kWaitBudget)) *abort_c = 1;
+                        if (!mbar_wait(bar_full + ((k + 1) & 1), ((k + 1) >> 1) & 1, kWaitBudget)) ab = true;
                         tc_fence_after();
-                        issue_x1(k + 1);
+                        if (!ab) issue_x1(k + 1);
                     }
                     tc_fence_after();
-                    issue_x2(k + 1);
+                    if (!ab) issue_x2(k + 1);
                 }
             }
             // outputs of block k (off the state's critical path)
@@ -812,8 +879,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (t + 1 < L) ob[(long)(t + 1) * p.Hv * DV] = __ushort_as_bfloat16((unsigned short)(opk[c] >> 16));
             }
         }
-        if (*abort_c || *abort_p) {
-            if (tid == kWG) flag_error(p.status);
+        if (failed) {
+            if (issuer) {  // nothing of this group may still be in flight when the CTA leaves
+                mma_commit(bar_fin_c);
+                mbar_wait(bar_fin_c, 0, kWaitBudget);
+                flag_error(p.status);
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < 64; j += 4)
@@ -822,6 +893,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     tc_fence_before();
     __syncthreads();
+    if (P > 1) cluster_sync();  // no CTA leaves while another may still touch its shared memory
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
@@ -863,6 +935,50 @@ bool prefill_tc_supported(const PrefillArgs &a) {
     return a.dtype == GDN_BF16 && a.dk == DK && a.dv == DV && a.chunk == C && Ttot > 0;
 }
 
+// CTAs per value head. The block chain of one head is sequential, but preparing a block
+// (norms, gates, the triangular solve, W) is not: with few heads the other SMs prepare blocks
+// for the state-carrying CTA of their cluster. P = 4 when every head's cluster fits on the
+// GPU at once, else 2, else 1; F = 1 (rank 0 only carries the state) needs P >= 3.
+// GDN_PREFILL_CLUSTER="P,F" overrides the choice (a tuning knob; invalid values are ignored).
+void pick_cluster(long heads, int *P, int *F) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    *P = 1;
+    *F = 0;
+    for (int cand : {4, 2}) {
+        if (heads * cand > sms) continue;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = cand;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)(heads * cand), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, prefill_tc_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (nclusters >= heads) {
+            *P = cand;
+            break;
+        }
+    }
+    *F = *P >= 3 ? 1 : 0;
+    if (const char *env = getenv("GDN_PREFILL_CLUSTER")) {
+        int pp = 0, ff = 0;
+        if (sscanf(env, "%d,%d", &pp, &ff) == 2 && (pp == 1 || pp == 2 || pp == 4) && (ff == 0 || (ff == 1 && pp >= 3))) {
+            *P = pp;
+            *F = ff;
+        }
+    }
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     const long Ttot = a.cu_seqlens ? (long)a.T : (long)a.B * a.T;
     CUtensorMap mq, mk, mv;
@@ -872,10 +988,27 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    int P = 1, F = 0;
+    pick_cluster((long)a.B * a.Hv, &P, &F);
     TcParams p{(const __nv_bfloat16 *)a.g, (const __nv_bfloat16 *)a.b, a.state_in, a.state_out,
-               (__nv_bfloat16 *)a.out, a.cu_seqlens, a.B, a.Hk, a.Hv, (long)a.T, Ttot, a.status};
-    prefill_tc_kernel<<<dim3(a.Hv, a.B), kThreads, SMEM_BYTES, s>>>(mq, mk, mv, p);
-    return cudaGetLastError();
+               (__nv_bfloat16 *)a.out, a.cu_seqlens, a.B, a.Hk, a.Hv, (long)a.T, Ttot, a.status, P, F};
+    if (P == 1) {
+        prefill_tc_kernel<<<dim3(a.Hv, a.B), kThreads, SMEM_BYTES, s>>>(mq, mk, mv, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = P;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(a.Hv * P), (unsigned)a.B, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mq, mk, mv, p);
 }
 
 }  // namespace gdn

@@ -74,6 +74,17 @@ def test_varlen_edges_qwen_heads(lengths):
         assert torch.equal(so[n].cpu(), b.state[n])
 
 
+@pytest.mark.parametrize("split", ["1,0", "2,0", "4,0", "4,1"])
+def test_cluster_splits(split, monkeypatch):
+    """With few heads, a cluster of P CTAs per value head prepares the blocks (ranks F..P-1 in
+    turn) for the CTA that carries the state: every split gives the oracle's result."""
+    monkeypatch.setenv("GDN_PREFILL_CLUSTER", split)
+    b = inputs.make_batch(Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", chunk=64, seed=21, init_state=True,
+                          slow_gate=True, lengths=[0, 1, 63, 64, 65, 130, 7, 700])
+    out, so = run_prefill(b)
+    check(b, out, so)
+
+
 def test_null_state_in_means_zeros():
     b = inputs.make_batch(B=1, T=130, Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", chunk=64, seed=6)
     out0, so0 = run_prefill(b, state_in=None)

@@ -72,7 +72,23 @@ constexpr uint32_t ST_W = 65536;    // 16 KiB MN-major [j 0..127][64 t] fp16, sc
 constexpr uint32_t ST_SC = 81920;   //  1 KiB block scalars (below)
 constexpr uint32_t STAGE = 82944;
 // stage scalars (float index)
-constexpr int SC_D = 0, SC_E = 64, SC_GAMMA = 128, SC_X1 = 129, SC_X2 = 130, SC_PO = 131, SC_L = 132;
+// SC_RK[t] = d_t rk_t and SC_RQ[t] = e_t rq_t turn raw K, Q rows into Kt, Qt; SC_SV = sig_v (V's scale)
+constexpr int SC_RK = 0, SC_RQ = 64, SC_GAMMA = 128, SC_X1 = 129, SC_X2 = 130, SC_PO = 131, SC_L = 132, SC_SV = 133;
+// What a helper sends when the state CTA converts the raw K, Q, V tiles itself: Tb, P, W and the scalars
+constexpr uint32_t ST_SENT = ST_TB, SENT_BYTES = STAGE - ST_TB;
+// A helper of a chain-only state CTA sends Tb as two bf16 tiles, Tb = hi + lo (hi = bf16(Tb),
+// lo = bf16(Tb - hi), about 16 significant bits), which multiply the raw bf16 V tile directly;
+// hi sits in the V region, which such a helper does not use, so the part sent is contiguous:
+// [Tb hi | Tb lo | P | W | scalars].
+constexpr uint32_t ST_TBH = ST_V + 8192;
+constexpr uint32_t ST_RSENT = ST_TBH, RSENT_BYTES = STAGE - ST_TBH;
+// shared memory of a chain-only state CTA (1 KiB aligned base as above)
+constexpr uint32_t CO_RAW = 0;                          // [2] raw K|Q (32 KiB) and V (16 KiB); Q rows to fp16
+constexpr uint32_t CO_RAW_BYTES = 49152;
+constexpr uint32_t CO_SENT = 2 * CO_RAW_BYTES;          // [3] what the helpers send
+constexpr uint32_t SN_TBH = ST_TBH - ST_RSENT, SN_TBL = ST_TB - ST_RSENT, SN_P = ST_P - ST_RSENT,
+                   SN_W = ST_W - ST_RSENT, SN_SC = ST_SC - ST_RSENT;
+constexpr uint32_t CO_SCL = CO_SENT + 3 * RSENT_BYTES;  // for O: row scales [2][128] x 2, P scale [2], L [2]
 // prep-private
 constexpr uint32_t RAW = 2 * STAGE;   // 48 KiB raw bf16 tiles: [kb][K rows 0..63 | Q rows 64..127] (32K), V (32K, 40K)
 constexpr uint32_t TW = RAW + 49152;  //  8 KiB [t][s] fp16, scaled Tw; solve scratch X before
@@ -83,9 +99,11 @@ constexpr int PS_G = 0, PS_BETA = 64, PS_AA = 128, PS_BB = 192, PS_EE = 256, PS_
 constexpr int RED_V = 0, RED_TP = 1, RED_W = 2;  // reduction sites
 constexpr uint32_t CSC = PSC + 4 * (PS_RED + 3 * 32);  // chain scratch: [2 sites][2 halves][128] floats
 constexpr uint32_t BAR = CSC + 4 * 512;
-constexpr uint32_t SMEM_USED = BAR + 128;
+constexpr uint32_t SMEM_USED = BAR + 256;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
 static_assert(SMEM_BYTES <= 232448, "over the 227 KiB opt-in limit");
+static_assert(CO_SCL + 4 * 528 <= CSC, "chain-only map overlaps the chain scratch");
+static_assert(RSENT_BYTES % 1024 == 0, "sent slots keep the 1 KiB swizzle alignment");
 
 // ---- TMEM columns (512 allocated) ----
 constexpr uint32_t TM_GW = 0;     // prep: Gram, then W^T          (64)
@@ -95,6 +113,11 @@ constexpr uint32_t TM_Q = 192;    // chain: S Qh^T                 (64)
 constexpr uint32_t TM_S = 256;    // chain: U~^T Kh                (128)
 constexpr uint32_t TM_AS = 384;   // chain: fp16 S, A operand      (64 = 128 fp16)
 constexpr uint32_t TM_AU = 448;   // chain: fp16 U^T               (32)
+// a state CTA that prepares no blocks (its cluster's other CTAs do) keeps Q and O apart
+// (X2 and O share columns: O(k) is issued after C has read X2(k), X2(k+1) after O has read O(k));
+// AUH/AUL: bf16 hi/lo of U diag(d rk) for the state update, AUF: fp16 U for the outputs
+constexpr uint32_t CT_X1 = 0, CT_X2O = 64, CT_Q = 128, CT_S = 192, CT_AS = 320, CT_AUH = 384, CT_AUL = 416,
+                   CT_AUF = 448;
 
 // instruction descriptor, kind::f16 with fp16 operands and an fp32 accumulator
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
@@ -108,6 +131,8 @@ constexpr uint32_t ID_X2 = idesc_f16(128, 64, 0, 1);
 constexpr uint32_t ID_Q = idesc_f16(128, 64, 0, 0);
 constexpr uint32_t ID_S = idesc_f16(128, 128, 0, 1);
 constexpr uint32_t ID_O = idesc_f16(128, 64, 0, 0);
+constexpr uint32_t ID_X1_BF16 = idesc_bf16(128, 64, 1, 0);   // raw V^T x Tb hi/lo
+constexpr uint32_t ID_S_BF16 = idesc_bf16(128, 128, 0, 1);   // U diag(d rk) hi/lo x raw K
 
 struct TcParams {
     const __nv_bfloat16 *g, *b;
@@ -146,6 +171,10 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
+}
+// bf16 operands, A from TMEM: the same instruction, the operand type is in the idesc
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    mma_f16_ts(d, a_tmem, b, idesc, acc);
 }
 // 32 lanes x 16 consecutive columns
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -263,6 +292,7 @@ __device__ void solve_unit_lower(const float *sA, float *sT, float *sX, int p, i
     }
 }
 
+template <bool kChainOnly>  // rank 0 carries the state and prepares no blocks (F = 1)
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -274,6 +304,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t *bar_tma = bars + 0, *bar_prep = bars + 1, *bar_full = bars + 2, *bar_empty = bars + 4;
     uint64_t *bar_x = bars + 6, *bar_fin_p = bars + 7, *bar_s = bars + 8, *bar_o = bars + 9;
     uint64_t *bar_fin_c = bars + 11;  // a group's last MMAs, waited for before leaving after a give-up
+    // handshakes of the state CTA when it prepares no blocks (kChainOnly)
+    uint64_t *bar_as = bars + 12;  // fp16 S for the next block stored (8 warps)
+    uint64_t *bar_u = bars + 13;   // [2] fp16 U of block k and the row scales stored (8 warps)
+    uint64_t *bar_of = bars + 15;  // [2] output accumulators of block k read (4 warps)
+    uint64_t *bar_tl = bars + 17;  // [2] raw K, Q, V tiles of raw slot k&1 loaded (TMA)
+    uint64_t *bar_rd = bars + 19;  // [2] block k complete: raw tiles converted, helper's part landed (3 warps)
+    uint64_t *bar_sent = bars + 21;  // [3] a helper's part landed in sent slot k%3 (bulk copy)
+    uint64_t *bar_uo = bars + 24;    // [2] fp16 U of block k and what O needs of block k stored (8 warps)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -297,6 +335,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
         mbar_init(bar_fin_c, 1);
+        mbar_init(bar_as, 8);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_u + s, 8);
+            mbar_init(bar_of + s, 4);
+            mbar_init(bar_tl + s, 1);
+            mbar_init(bar_rd + s, 3);
+            mbar_init(bar_uo + s, 8);
+        }
+        for (int j = 0; j < 3; ++j) mbar_init(bar_sent + j, 1);
+        if (kChainOnly && rank == 0)
+            for (int j = 0; j < 5; ++j) reinterpret_cast<int *>(sm + CO_SCL + 4 * 516)[j] = 0;  // load/release counts
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_slot, 512);
@@ -309,7 +358,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int half = (tid >> 7) & 1;                              // which half of a row this thread owns
     const int r = tid & 127;                                      // TMEM lane = row
 
-    if (tid < kWG && rank >= F) {
+    if (tid < kWG && rank >= F && !(kChainOnly && rank == 0)) {
         // ======================= prep =======================
         // This CTA prepares blocks first, first + NP, ...; rank 0 writes them straight into its
         // stage k & 1, the other ranks into a local buffer (alternating two) that one bulk copy
@@ -317,6 +366,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int pt = tid;
         const int first = rank - F;
         const bool local = rank == 0;
+        // helpers of a chain-only state CTA leave Kt, Qt and V to it (it loads the raw tiles itself)
+        const bool send_raw = kChainOnly && !local;
         uint32_t nwait[2] = {0u, 0u};  // completed waits on empty[0], empty[1]
         // Every wait gives up after kWaitBudget cycles and sets `ab` in the waiting thread; the group
         // leaves the loop together at the next bar_any. Tiles requested and not yet waited for are
@@ -457,19 +508,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ++nwait[s];
                 if (bar_any(1, kWG, ab)) { failed = true; break; }
             }
+            if (!send_raw || r < 64) {  // Kh rows (W needs them here), Qt rows
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float x[8];
-                unpack8(raw8[c], x);
-                *reinterpret_cast<uint4 *>(st + ST_KQ + half * 16384 + swz(r, c)) = pack8_f16(x, qscale);
+                for (int c = 0; c < 8; ++c) {
+                    float x[8];
+                    unpack8(raw8[c], x);
+                    *reinterpret_cast<uint4 *>(st + ST_KQ + half * 16384 + swz(r, c)) = pack8_f16(x, qscale);
+                }
             }
+            if (!send_raw) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = vq + cc;
-                float x[8];
-                unpack8(rawv[cc], x);
-                *reinterpret_cast<uint4 *>(st + ST_V + (c >> 3) * 8192 + swz(vt, c & 7)) =
-                    pack8_f16(x, vt < L ? sig_v : 0.f);
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = vq + cc;
+                    float x[8];
+                    unpack8(rawv[cc], x);
+                    *reinterpret_cast<uint4 *>(st + ST_V + (c >> 3) * 8192 + swz(vt, c & 7)) =
+                        pack8_f16(x, vt < L ? sig_v : 0.f);
+                }
             }
             fence_async_smem();
             tc_fence_before();
@@ -562,7 +617,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float sig_b = pow2_scale(mbb), sig_w = pow2_scale(mww), sig_p = pow2_scale(mpp);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
-                *reinterpret_cast<uint4 *>(st + ST_TB + swz(tt, 2 * q + cc)) = pack8_f16(&tb[8 * cc], sig_b);
+                if (send_raw) {  // Tb = hi + lo in bf16, unscaled
+                    float lo[8];
+                    const uint4 hi = pack8(&tb[8 * cc]);
+                    float hv[8];
+                    unpack8(hi, hv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) lo[e] = tb[8 * cc + e] - hv[e];
+                    *reinterpret_cast<uint4 *>(st + ST_TBH + swz(tt, 2 * q + cc)) = hi;
+                    *reinterpret_cast<uint4 *>(st + ST_TB + swz(tt, 2 * q + cc)) = pack8(lo);
+                } else {
+                    *reinterpret_cast<uint4 *>(st + ST_TB + swz(tt, 2 * q + cc)) = pack8_f16(&tb[8 * cc], sig_b);
+                }
                 *reinterpret_cast<uint4 *>(sm + TW + swz(tt, 2 * q + cc)) = pack8_f16(&tw[8 * cc], sig_w);
             }
             if (r >= 64) {
@@ -606,7 +672,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     *reinterpret_cast<uint4 *>(st + ST_W + swz(r, 4 * half + cc)) = pack8_f16(&w0[8 * cc], f);
                     *reinterpret_cast<uint4 *>(st + ST_W + swz(r, 4 * half + 2 + cc)) = pack8_f16(&w1[8 * cc], f);
                 }
-                {  // thread (row r < 64 of Kh, K-block half): scale by d_r in place
+                if (!send_raw) {  // thread (row r < 64 of Kh, K-block half): scale by d_r in place
                     const int kr = r & 63, kh = (r >> 6) + 2 * half;  // 64 rows x 4 chunk groups
                     const float dr = ps[PS_DD + kr];
 #pragma unroll
@@ -625,14 +691,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                 }
                 if (pt < C) {
-                    stsc[SC_D + pt] = ps[PS_DD + pt];
-                    stsc[SC_E + pt] = ps[PS_EE + pt];
+                    stsc[SC_RK + pt] = ps[PS_DD + pt] * ps[PS_RK + pt];
+                    stsc[SC_RQ + pt] = ps[PS_EE + pt] * ps[PS_RQ + pt];
                 }
                 if (pt == 0) {
                     stsc[SC_GAMMA] = expf(GL);
-                    stsc[SC_X1] = 1.f / (sig_v * sig_b);
+                    stsc[SC_X1] = send_raw ? 1.f : 1.f / (sig_v * sig_b);
                     stsc[SC_X2] = 1.f / sig_ww;
                     stsc[SC_PO] = 1.f / sig_p;
+                    stsc[SC_SV] = sig_v;
                     reinterpret_cast<int *>(stsc)[SC_L] = L;
                 }
             }
@@ -641,6 +708,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bar_sync(1, kWG);
             if (local) {
                 if (pt == 0) mbar_arrive(bar_full + s);
+            } else if (pt == 0 && send_raw) {
+                // Tb, P, W and the scalars go to rank 0's sent slot k % 3, which is free once block
+                // k-3 is consumed; one producer per slot (NP = 3), so the releases come in order.
+                // (This buffer was last copied out two jobs ago, block k-6; the previous job's wait,
+                // block k-6 consumed, already implied that copy had landed.)
+                bool ok = true;
+                if (k >= 3) {
+                    ok = mbar_wait_cluster(bar_empty, nwait[0] & 1, kWaitBudget);
+                    ++nwait[0];
+                }
+                if (!ok) {
+                    ab = true;
+                } else {
+                    const uint32_t j = (uint32_t)(k % 3);
+                    const uint32_t full_r = mapa_shared(smem_u32(bar_sent + j), 0);
+                    mbar_arrive_expect_tx_cluster(full_r, RSENT_BYTES);
+                    bulk_copy_to_cluster(mapa_shared(sb + CO_SENT + j * RSENT_BYTES, 0), st + ST_RSENT, RSENT_BYTES, full_r);
+                }
             } else if (pt == 0) {
                 // rank 0's stage s is free once the chain has finished block k-2. (This buffer was last
                 // copied out two jobs ago, block k - 2 NP; the previous job's wait, block k - NP - 2
@@ -668,6 +753,341 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mma_commit(bar_fin_p);
             mbar_wait(bar_fin_p, 0, kWaitBudget);
             flag_error(p.status);
+        }
+    } else if (kChainOnly && rank == 0) {
+        // ============ state CTA of a cluster whose other CTAs prepare every block ============
+        // Issuing tcgen05.mma holds the issuing thread until the tensor pipe has nearly finished
+        // the batch, and a cluster-scope arrive waits for the thread's own outstanding global
+        // stores; so each job has its own threads:
+        //   C (threads 256..511): the state, two threads per row as above, waits on mbarriers only;
+        //   I (thread 0): issues every MMA;
+        //   O (threads 128..255, one row each): the bf16 outputs; its first thread also starts the
+        //     raw tile loads of block k+2 and returns block k's sent slot once block k's MMAs are done;
+        //   M (threads 32..127): converts the Q rows of each raw tile to Qt in fp16.
+        // Operands between SMs move at about 21 B per cycle, TMA from L2 much faster, so the raw
+        // K, Q, V tiles come by TMA and a helper sends only Tb (hi, lo), P, W and the scalars (41 KiB)
+        // into one of three sent slots: its copy has two block periods to land. K and V are used raw
+        // (bf16): Tb and U diag(d rk) are split into bf16 hi + lo to multiply them.
+        // Per block k:  I: X1(k) X2(k) Q(k) -> C: U(k) -> I: S(k), O(k) -> C: state update, fp16 S(k+1)
+        //   -> I: X1(k+1) X2(k+1) Q(k+1);  O: outputs of block k, loads block k+2.
+        float *sgs = reinterpret_cast<float *>(sm + CO_SCL);  // [2][128] row scale of fp16 S(k)
+        float *sgu = sgs + 256;                               // [2][128] row scale of fp16 U(k)
+        float *spo = sgu + 256;                               // [2] P scale; [2] L (as int)
+        int *req = reinterpret_cast<int *>(spo + 4);          // [2] raw loads requested per raw slot, [3] releases per sent slot
+        auto raw_b = [&](int k) { return sb + CO_RAW + (uint32_t)(k & 1) * CO_RAW_BYTES; };
+        auto sent_b = [&](int k) { return sb + CO_SENT + (uint32_t)(k % 3) * RSENT_BYTES; };
+        auto load_raw = [&](int k) {  // raw bf16 K, Q, V tiles of block k into raw slot k&1
+            uint8_t *rs = sm + CO_RAW + (k & 1) * CO_RAW_BYTES;
+            const int c_tok = (int)(bos + (long)k * C);
+            mbar_expect_tx(bar_tl + (k & 1), 6 * 8192);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_3d(rs + ST_KQ + kb * 16384, &tm_k, kb * 64, hk, c_tok, bar_tl + (k & 1));
+                tma_load_3d(rs + ST_KQ + kb * 16384 + 8192, &tm_q, kb * 64, hk, c_tok, bar_tl + (k & 1));
+                tma_load_3d(rs + ST_V + kb * 8192, &tm_v, kb * 64, h, c_tok, bar_tl + (k & 1));
+            }
+            ++req[k & 1];
+        };
+        if (tid == 0) {
+            // ---------------- I ----------------
+            bool ab = false;
+            auto iwait = [&](uint64_t *bar, uint32_t ph) {
+                if (!ab && !mbar_wait_spin(bar, ph, kWaitBudget)) ab = true;
+                if (!ab) tc_fence_after();
+                return !ab;
+            };
+            auto issue_x1 = [&](int k) {  // V^T (Tb hi + Tb lo)^T
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t a = desc_sw128(raw_b(k) + ST_V + ks * 2048, 8192, 1024);
+                    mma_bf16(tmem + CT_X1, a, desc_sw128(sent_b(k) + SN_TBH + ks * 32, 16, 1024), ID_X1_BF16, ks > 0);
+                    mma_bf16(tmem + CT_X1, a, desc_sw128(sent_b(k) + SN_TBL + ks * 32, 16, 1024), ID_X1_BF16, 1);
+                }
+            };
+            auto issue_x2 = [&](int k) {  // S (-W)^T
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_f16_ts(tmem + CT_X2O, tmem + CT_AS + 8 * ks,
+                               desc_sw128(sent_b(k) + SN_W + ks * 2048, 8192, 1024), ID_X2, ks > 0);
+                mma_commit(bar_x);
+            };
+            auto issue_q = [&](int k) {  // S Qt^T
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_f16_ts(tmem + CT_Q, tmem + CT_AS + 8 * ks,
+                               desc_sw128(raw_b(k) + ST_KQ + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024), ID_Q,
+                               ks > 0);
+            };
+            if (nchunks > 0) {
+                if (iwait(bar_rd, 0)) issue_x1(0);
+                if (iwait(bar_as, 0)) {
+                    issue_x2(0);
+                    issue_q(0);
+                }
+            }
+            for (int k = 0; k < nchunks && !ab; ++k) {
+                if (!iwait(bar_u + (k & 1), (k >> 1) & 1)) break;  // U diag(d rk) hi/lo stored; X1(k), X2(k) read
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {  // (hi + lo)^T K
+                    const uint64_t b = desc_sw128(raw_b(k) + ST_KQ + ks * 2048, 16384, 1024);
+                    mma_bf16_ts(tmem + CT_S, tmem + CT_AUH + 8 * ks, b, ID_S_BF16, ks > 0);
+                    mma_bf16_ts(tmem + CT_S, tmem + CT_AUL + 8 * ks, b, ID_S_BF16, 1);
+                }
+                mma_commit(bar_s);
+                if (!iwait(bar_uo + (k & 1), (k >> 1) & 1)) break;  // fp16 U stored
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)  // U^T P^T
+                    mma_f16_ts(tmem + CT_X2O, tmem + CT_AUF + 8 * ks, desc_sw128(sent_b(k) + SN_P + ks * 32, 16, 1024),
+                               ID_O, ks > 0);
+                mma_commit(bar_o);  // every MMA of block k
+                if (k + 1 < nchunks) {
+                    if (!iwait(bar_rd + ((k + 1) & 1), ((k + 1) >> 1) & 1)) break;
+                    issue_x1(k + 1);
+                    if (!iwait(bar_as, (k + 1) & 1)) break;             // fp16 S(k+1) stored
+                    if (!iwait(bar_of + (k & 1), (k >> 1) & 1)) break;  // O(k) and Q(k) read
+                    issue_x2(k + 1);
+                    issue_q(k + 1);
+                }
+            }
+            mma_commit(bar_fin_c);  // nothing issued here may still run when the CTA leaves
+            mbar_wait(bar_fin_c, 0, kWaitBudget);
+            if (ab) flag_error(p.status);
+        } else if (tid >= 32 && tid < 128) {
+            // ---------------- M ----------------
+            bool ab = false, failed = false;
+            if (tid == 32) {
+                prefetch_tmap(&tm_q);
+                prefetch_tmap(&tm_k);
+                prefetch_tmap(&tm_v);
+                for (int k = 0; k < 2 && k < nchunks; ++k) load_raw(k);
+            }
+            for (int k = 0; k < nchunks; ++k) {
+                if (!ab && !mbar_wait(bar_tl + (k & 1), (k >> 1) & 1, kWaitBudget)) ab = true;
+                if (!ab && !mbar_wait(bar_sent + k % 3, (k / 3) & 1, kWaitBudget)) ab = true;
+                if (bar_any(4, 96, ab)) {
+                    failed = true;
+                    break;
+                }
+                uint8_t *rs = sm + CO_RAW + (k & 1) * CO_RAW_BYTES;
+                const float *stsc = reinterpret_cast<const float *>(sm + CO_SENT + (k % 3) * RSENT_BYTES + SN_SC);
+                // Q rows 64..127 of the two 64-column halves: 1024 chunks of 16 B, consecutive threads on
+                // consecutive chunks (row = chunk / 8; the swizzle only permutes chunks within a row)
+#pragma unroll
+                for (int i0 = 0; i0 < 11; i0 += 4) {
+                    uint4 v[4];
+                    float f[4];
+                    uint32_t off[4];
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const int m = (tid - 32) + 96 * (i0 + ii);
+                        const int row = 64 + ((m >> 3) & 63);
+                        off[ii] = (uint32_t)((m >> 9) * 16384 + row * 128 + (m & 7) * 16);
+                        f[ii] = stsc[SC_RQ + row - 64];
+                        if (m < 1024) v[ii] = *reinterpret_cast<const uint4 *>(rs + off[ii]);
+                    }
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const int m = (tid - 32) + 96 * (i0 + ii);
+                        if (m < 1024) {
+                            float x[8];
+                            unpack8(v[ii], x);
+                            *reinterpret_cast<uint4 *>(rs + off[ii]) =
+                                f[ii] != 0.f ? pack8_f16(x, f[ii]) : make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_rd + (k & 1));
+            }
+            if (failed && tid == 32) flag_error(p.status);
+        } else if (tid >= 128 && tid < kWG) {
+            // ---------------- O ----------------
+            const int i = tid & 127;
+            bool ab = false, failed = false;
+            for (int k = 0; k < nchunks; ++k) {
+                const long c0 = bos + (long)k * C;
+                if (!ab && !mbar_wait(bar_o, k & 1, kWaitBudget)) ab = true;
+                if (!ab && !mbar_wait(bar_uo + (k & 1), (k >> 1) & 1, kWaitBudget)) ab = true;  // scales from C
+                __syncwarp();
+                tc_fence_after();
+                const float fq = 1.f / sgs[(k & 1) * 128 + i], fo = spo[k & 1] / sgu[(k & 1) * 128 + i];
+                const int L = reinterpret_cast<const int *>(spo)[2 + (k & 1)];
+                uint32_t opk[32];  // outputs t = 0..63 of row i, bf16 pairs
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t qa[16], oa[16];
+                    tmem_ld16_nw(tmem + CT_Q + lane_off + 16 * q, qa);
+                    tmem_ld16_nw(tmem + CT_X2O + lane_off + 16 * q, oa);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float o0 = __uint_as_float(qa[2 * c]) * fq + __uint_as_float(oa[2 * c]) * fo;
+                        const float o1 = __uint_as_float(qa[2 * c + 1]) * fq + __uint_as_float(oa[2 * c + 1]) * fo;
+                        opk[8 * q + c] = bf2_bits(__floats2bfloat162_rn(o0, o1));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_of + (k & 1));
+                if (tid == 128 && !ab) {
+                    // every MMA of block k is done (bar_o) and C read its scalars before fp16 U (bar_uo);
+                    // M read them before block k was ready: raw slot k&1 and sent slot k%3 are free
+                    if (k + 2 < nchunks) load_raw(k + 2);
+                    if (k + 3 < nchunks) {
+                        ++req[2 + k % 3];
+                        mbar_arrive_cluster(mapa_shared(smem_u32(bar_empty), (uint32_t)(F + (k + 3) % NP)));
+                    }
+                }
+                if (bar_any(3, 128, ab)) {
+                    failed = true;
+                    break;
+                }
+                __nv_bfloat16 *ob = p.out + (c0 * p.Hv + h) * (long)DV + i;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int t = 2 * c;
+                    if (t < L) ob[(long)t * p.Hv * DV] = __ushort_as_bfloat16((unsigned short)(opk[c] & 0xffffu));
+                    if (t + 1 < L) ob[(long)(t + 1) * p.Hv * DV] = __ushort_as_bfloat16((unsigned short)(opk[c] >> 16));
+                }
+            }
+            if (failed && tid == 128) flag_error(p.status);
+        } else if (tid >= kWG) {
+            // ---------------- C ----------------
+            const int i = r;
+            float *cx = reinterpret_cast<float *>(sm + CSC);
+            float S[64];
+            const long st_off = ((long)n * p.Hv + h) * (long)DV * DK + (long)i * DK + 64 * half;
+            if (p.state_in) {
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(p.state_in + st_off + j);
+                    S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) S[j] = 0.f;
+            }
+            bool ab = false, failed = false;
+            auto cwait = [&](uint64_t *bar, uint32_t ph) {
+                if (!ab && !mbar_wait_spin(bar, ph, kWaitBudget)) ab = true;
+                __syncwarp();
+                tc_fence_after();
+            };
+            auto warp_arrive = [&](uint64_t *bar) {  // this warp's TMEM stores (and smem writes) are done
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar);
+            };
+            auto row_scale = [&](float m, int site) {
+                cx[site * 256 + half * 128 + i] = m;
+                bar_sync(2, kWG);
+                return pow2_scale(fmaxf(cx[site * 256 + i], cx[site * 256 + 128 + i]));
+            };
+            auto smax = [&]() {
+                float m = 0.f;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) m = fmaxf(m, fabsf(S[j]));
+                return m;
+            };
+            auto store_state_f16 = [&](float sc) {
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t rr[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) rr[c] = h2_bits(sc * S[16 * c8 + 2 * c], sc * S[16 * c8 + 2 * c + 1]);
+                    tmem_st8(tmem + CT_AS + lane_off + 32 * half + 8 * c8, rr);
+                }
+            };
+            float sig_s = row_scale(smax(), 0);
+            if (nchunks > 0) {
+                store_state_f16(sig_s);
+                warp_arrive(bar_as);
+            }
+            for (int k = 0; k < nchunks; ++k) {
+                const float *stsc = reinterpret_cast<const float *>(sm + CO_SENT + (k % 3) * RSENT_BYTES + SN_SC);
+                cwait(bar_rd + (k & 1), (k >> 1) & 1);  // block k's scalars (long since there)
+                cwait(bar_x, k & 1);                     // X1(k), X2(k)
+                const float f1 = stsc[SC_X1], f2 = stsc[SC_X2] / sig_s, gam = stsc[SC_GAMMA];
+                float u[32];  // U^T[i][t], t in [32 half, 32 half + 32)
+                float m = 0.f;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t a[16], bx[16];
+                    tmem_ld16_nw(tmem + CT_X1 + lane_off + 32 * half + 16 * q, a);
+                    tmem_ld16_nw(tmem + CT_X2O + lane_off + 32 * half + 16 * q, bx);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) u[16 * q + e] = __uint_as_float(a[e]) * f1 + __uint_as_float(bx[e]) * f2;
+                }
+                // the state update's operand first: U diag(d rk) as bf16 hi + lo (no scaling needed)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t rh[8], rl[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int e = 16 * q + 2 * c;
+                        const float x0 = u[e] * stsc[SC_RK + 32 * half + e], x1 = u[e + 1] * stsc[SC_RK + 32 * half + e + 1];
+                        const __nv_bfloat162 hb = __floats2bfloat162_rn(x0, x1);
+                        const float2 hf = __bfloat1622float2(hb);
+                        rh[c] = bf2_bits(hb);
+                        rl[c] = bf2_bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
+                    }
+                    tmem_st8(tmem + CT_AUH + lane_off + 16 * half + 8 * q, rh);
+                    tmem_st8(tmem + CT_AUL + lane_off + 16 * half + 8 * q, rl);
+                }
+                warp_arrive(bar_u + (k & 1));
+                // then fp16 U for the outputs (row scale), and what O needs of this block
+#pragma unroll
+                for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(u[e]));
+                const float sig_u = row_scale(m, 1);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t ru[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) ru[c] = h2_bits(sig_u * u[16 * q + 2 * c], sig_u * u[16 * q + 2 * c + 1]);
+                    tmem_st8(tmem + CT_AUF + lane_off + 16 * half + 8 * q, ru);
+                }
+                if (half == 0) {
+                    sgs[(k & 1) * 128 + i] = sig_s;
+                    sgu[(k & 1) * 128 + i] = sig_u;
+                }
+                if (tid == kWG) {
+                    spo[k & 1] = stsc[SC_PO];
+                    reinterpret_cast<int *>(spo)[2 + (k & 1)] = reinterpret_cast<const int *>(stsc)[SC_L];
+                }
+                warp_arrive(bar_uo + (k & 1));
+                cwait(bar_s, k & 1);  // (hi + lo)^T K
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t d0[16], d1[16];
+                    tmem_ld16_nw(tmem + CT_S + lane_off + 64 * half + 32 * q2, d0);
+                    tmem_ld16_nw(tmem + CT_S + lane_off + 64 * half + 32 * q2 + 16, d1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        S[32 * q2 + e] = gam * S[32 * q2 + e] + __uint_as_float(d0[e]);
+                        S[32 * q2 + 16 + e] = gam * S[32 * q2 + 16 + e] + __uint_as_float(d1[e]);
+                    }
+                }
+                sig_s = row_scale(smax(), 0);
+                if (k + 1 < nchunks) {
+                    store_state_f16(sig_s);
+                    warp_arrive(bar_as);
+                }
+                if (bar_any(2, kWG, ab)) {
+                    failed = true;
+                    break;
+                }
+            }
+            if (failed) {
+                if (tid == kWG) flag_error(p.status);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; j += 4)
+                    *reinterpret_cast<float4 *>(p.state_out + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            }
         }
     } else if (tid >= kWG && rank == 0) {
         // ======================= chain =======================
@@ -894,6 +1314,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_before();
     __syncthreads();
     if (P > 1) cluster_sync();  // no CTA leaves while another may still touch its shared memory
+    if (kChainOnly) {
+        // After a give-up, raw loads and helper copies may still be in flight into the state CTA; they
+        // land (bounded waits) before any CTA of the cluster leaves. At most one is outstanding per slot.
+        if (rank == 0 && tid == 32) {
+            const int *req = reinterpret_cast<const int *>(sm + CO_SCL + 4 * 516);
+            for (int s = 0; s < 2; ++s)
+                if (req[s] > 0) mbar_wait(bar_tl + s, (uint32_t)(req[s] - 1) & 1, kWaitBudget);
+            for (int j = 0; j < 3; ++j) {
+                const int ncp = (j < nchunks ? 1 : 0) + req[2 + j];
+                if (ncp > 0) mbar_wait(bar_sent + j, (uint32_t)(ncp - 1) & 1, kWaitBudget);
+            }
+        }
+        __syncthreads();
+        cluster_sync();
+    }
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
@@ -960,7 +1395,7 @@ void pick_cluster(long heads, int *P, int *F) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int nclusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, prefill_tc_kernel, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&nclusters, prefill_tc_kernel<false>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             continue;
         }
@@ -985,15 +1420,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     if (!make_map(&mq, a.q, DK, a.Hk, Ttot) || !make_map(&mk, a.k, DK, a.Hk, Ttot) ||
         !make_map(&mv, a.v, DV, a.Hv, Ttot))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {prefill_tc_kernel<false>, prefill_tc_kernel<true>}) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+    }
     int P = 1, F = 0;
     pick_cluster((long)a.B * a.Hv, &P, &F);
     TcParams p{(const __nv_bfloat16 *)a.g, (const __nv_bfloat16 *)a.b, a.state_in, a.state_out,
                (__nv_bfloat16 *)a.out, a.cu_seqlens, a.B, a.Hk, a.Hv, (long)a.T, Ttot, a.status, P, F};
     if (P == 1) {
-        prefill_tc_kernel<<<dim3(a.Hv, a.B), kThreads, SMEM_BYTES, s>>>(mq, mk, mv, p);
+        prefill_tc_kernel<false><<<dim3(a.Hv, a.B), kThreads, SMEM_BYTES, s>>>(mq, mk, mv, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -1008,7 +1444,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mq, mk, mv, p);
+    return F ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, mq, mk, mv, p)
+             : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, mq, mk, mv, p);
 }
 
 }  // namespace gdn

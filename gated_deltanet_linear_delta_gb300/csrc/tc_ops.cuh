@@ -65,6 +65,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase, long lo
     return true;
 }
 
+// Same, without the suspend hint: for a thread on the critical path that has nothing else to do.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t phase, long long budget) {
+    if (mbar_try_wait(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, phase))
+        if (clock64() - t0 > budget) return false;
+    return true;
+}
+
 // ---- thread-block clusters (distributed shared memory) ----------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -982,7 +982,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             };
             auto row_scale = [&](float m, int site) {
                 cx[site * 256 + half * 128 + i] = m;
-                bar_sync(2, kWG);
+                bar_sync(6 + (warp & 3), 64);  // the two halves of a row sit in warps w and w+4
                 return pow2_scale(fmaxf(cx[site * 256 + i], cx[site * 256 + 128 + i]));
             };
             auto smax = [&]() {

@@ -250,12 +250,14 @@ __device__ void solve_unit_lower(const float *sA, float *sT, float *sX, int p, i
     // Level d (blocks i = j + d): X_ij = sum_{k=j}^{i-1} A_ik T_kj, T_ij = -T_ii X_ij.
     // The X phase gives each (block, term k) its own 64 threads (4 adjacent outputs each), so
     // 192..256 threads work in every phase; the T phase adds the d partial products.
-#pragma unroll
+    // One copy of the level code (instruction fetch is a shared, contended resource when every
+    // SM runs this), with the (block, term) split done without a division.
+#pragma unroll 1
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;                   // blocks in this level
         const int slot = p >> 6;                // (block, term) pair handled by this thread
         const bool act = slot < nb * d;
-        const int blk = slot / d, kk = slot % d;
+        const int blk = d == 1 ? slot : (d == 2 ? slot >> 1 : 0), kk = slot - blk * d;
         const int r = (p >> 2) & 15, c0 = (p & 3) * 4;
         if (act) {
             const int i = d + blk, j = blk, k = j + kk;
@@ -280,9 +282,11 @@ __device__ void solve_unit_lower(const float *sA, float *sT, float *sX, int p, i
                 const float a = sT[sw(16 * i + r, 16 * i + m)];
                 float4 x4 = *reinterpret_cast<const float4 *>(sX + (tb * d) * 256 + m * 16 + c0);
 #pragma unroll
-                for (int q = 1; q < d; ++q) {
-                    const float4 y4 = *reinterpret_cast<const float4 *>(sX + (tb * d + q) * 256 + m * 16 + c0);
-                    x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
+                for (int q = 1; q < 3; ++q) {
+                    if (q < d) {
+                        const float4 y4 = *reinterpret_cast<const float4 *>(sX + (tb * d + q) * 256 + m * 16 + c0);
+                        x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
+                    }
                 }
                 acc.x += a * x4.x; acc.y += a * x4.y; acc.z += a * x4.z; acc.w += a * x4.w;
             }
@@ -797,7 +801,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 return !ab;
             };
             auto issue_x1 = [&](int k) {  // V^T (Tb hi + Tb lo)^T
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t a = desc_sw128(raw_b(k) + ST_V + ks * 2048, 8192, 1024);
                     mma_bf16(tmem + CT_X1, a, desc_sw128(sent_b(k) + SN_TBH + ks * 32, 16, 1024), ID_X1_BF16, ks > 0);
@@ -805,14 +809,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             };
             auto issue_x2 = [&](int k) {  // S (-W)^T
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
                     mma_f16_ts(tmem + CT_X2O, tmem + CT_AS + 8 * ks,
                                desc_sw128(sent_b(k) + SN_W + ks * 2048, 8192, 1024), ID_X2, ks > 0);
                 mma_commit(bar_x);
             };
             auto issue_q = [&](int k) {  // S Qt^T
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
                     mma_f16_ts(tmem + CT_Q, tmem + CT_AS + 8 * ks,
                                desc_sw128(raw_b(k) + ST_KQ + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024), ID_Q,
@@ -827,7 +831,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             for (int k = 0; k < nchunks && !ab; ++k) {
                 if (!iwait(bar_u + (k & 1), (k >> 1) & 1)) break;  // U diag(d rk) hi/lo stored; X1(k), X2(k) read
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {  // (hi + lo)^T K
                     const uint64_t b = desc_sw128(raw_b(k) + ST_KQ + ks * 2048, 16384, 1024);
                     mma_bf16_ts(tmem + CT_S, tmem + CT_AUH + 8 * ks, b, ID_S_BF16, ks > 0);
@@ -835,7 +839,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 mma_commit(bar_s);
                 if (!iwait(bar_uo + (k & 1), (k >> 1) & 1)) break;  // fp16 U stored
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks)  // U^T P^T
                     mma_f16_ts(tmem + CT_X2O, tmem + CT_AUF + 8 * ks, desc_sw128(sent_b(k) + SN_P + ks * 32, 16, 1024),
                                ID_O, ks > 0);

@@ -199,6 +199,7 @@ def run_ours(args, rank, world):
         us = 1e3 * sum(a.elapsed_time(b) for a, b in times) / len(times)
         sweep[str(n)] = round(us, 3)
 
+    graph = decode_graph_sweep(gdn, (qd, kd, vd, gd, bd), dstate, dout, stream)
     e2e = measure_e2e(args, gdn, pb, dec, dev, stream)
     hbm, bf16, src = peaks()
     pre_s = pre_mean / 1e3
@@ -228,7 +229,7 @@ def run_ours(args, rank, world):
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                                 "frac": round(dec_gbs / hbm, 4), "traffic": TRAFFIC["decode"],
                                 "peak_source": src},
-                   "sweep_us": sweep},
+                   "sweep_us": sweep, "graph": graph},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC["prefill"], "peak_source": src,
                      "kernel": "prefill"},
@@ -238,6 +239,43 @@ def run_ours(args, rank, world):
         "wall_s_timed_region": round(wall, 4),
     }
     return line
+
+
+def decode_graph_sweep(gdn, qkvgb, dstate, dout, stream, G=32, reps=20):
+    """Decode steps back to back (the state updated in place, L2 warm): G launches issued eagerly
+    against the same G launches captured once in a CUDA graph and replayed; us per step."""
+    qd, kd, vd, gd, bd = qkvgb
+    res = {"steps_per_graph": G, "l2": "warm (consecutive steps, no flush)"}
+    for n in (1, 8, 32, 128):
+        def steps():
+            for _ in range(G):
+                gdn.gdn_decode_step(qd[:n], kd[:n], vd[:n], gd[:n], bd[:n], dstate[:n], dout[:n])
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            steps()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            steps()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                steps()
+                graph.replay()
+            ev[0].record(stream)
+            for _ in range(reps):
+                steps()
+            ev[1].record(stream)
+            ev[2].record(stream)
+            for _ in range(reps):
+                graph.replay()
+            ev[3].record(stream)
+        torch.cuda.synchronize()
+        res[str(n)] = {"eager_us": round(1e3 * ev[0].elapsed_time(ev[1]) / (reps * G), 3),
+                       "graph_us": round(1e3 * ev[2].elapsed_time(ev[3]) / (reps * G), 3)}
+        del graph
+    return res
 
 
 def measure_e2e(args, gdn, pb, dec, dev, stream):

@@ -20,7 +20,7 @@ import torch
 
 from . import _build
 
-__all__ = ["GDNError", "gdn_prefill", "gdn_decode_step", "gdn_prepass", "gdn_prefill_path",
+__all__ = ["GDNError", "gdn_prefill", "gdn_decode_step", "gdn_decode_step_slots", "gdn_prepass", "gdn_prefill_path",
            "gdn_get_device_status", "gdn_status_string", "library", "library_path",
            "GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
            "GDN_ERR_DEVICE_CHECK", "GDN_BF16", "GDN_F32"]
@@ -58,6 +58,8 @@ def library() -> ctypes.CDLL:
             lib.gdn_prefill.restype = _I
             lib.gdn_decode_step.argtypes = [_P] * 7 + [_I] * 6 + [_P]
             lib.gdn_decode_step.restype = _I
+            lib.gdn_decode_step_slots.argtypes = [_P] * 8 + [_I] * 7 + [_P]
+            lib.gdn_decode_step_slots.restype = _I
             lib.gdn_prepass.argtypes = [_P] * 5 + [_I] * 7 + [_P] * 4 + [_P]
             lib.gdn_prepass.restype = _I
             lib.gdn_prefill_path.argtypes = [_I] * 8
@@ -136,6 +138,20 @@ def gdn_decode_step(q, k, v, g, b, state, out, stream=None) -> None:
     rc = library().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state), _ptr(out),
                                    N, Hk, Hv, dk, dv, dt, _stream(stream))
     _check(rc, "gdn_decode_step")
+
+
+def gdn_decode_step_slots(q, k, v, g, b, state_pool, slots, out, stream=None) -> None:
+    """One decode step; sequence n updates state_pool[slots[n]] in place (slots[n] < 0: padding)."""
+    N, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    if state_pool.dtype != torch.float32:
+        raise TypeError("the state pool is fp32")
+    if slots.dtype != torch.int32 or slots.numel() != N:
+        raise TypeError("slots must be int32 with one entry per sequence")
+    rc = library().gdn_decode_step_slots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_pool),
+                                         _ptr(slots), _ptr(out), N, state_pool.shape[0], Hk, Hv, dk, dv,
+                                         _dtype_code(q), _stream(stream))
+    _check(rc, "gdn_decode_step_slots")
 
 
 def gdn_prepass(q, k, g, b, rq, rk, beta, gcum, cu_seqlens=None, B=None, T=None, chunk=64,

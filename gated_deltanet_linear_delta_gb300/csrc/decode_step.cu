@@ -23,6 +23,13 @@
 // before any arithmetic so that 16*R bytes per thread are in flight. All rows
 // of one warp belong to one (sequence, head), so the norms are computed once
 // per warp.
+//
+// Slot-indexed variant (kSlots): the states live in a pool of `num_slots`
+// [Hv][dv][dk] entries and sequence n updates pool entry slots[n], so a server
+// can keep many sessions resident and step any subset of them in one launch.
+// A negative slot marks a padding row (state untouched, output zero); a slot
+// >= num_slots is a caller error, flagged on the device status word and
+// skipped the same way.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -32,11 +39,12 @@ namespace {
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeRows = 4;  // passes (rows per lane group) per warp
 
-template <int DK, int DV, typename TIn>
+template <int DK, int DV, typename TIn, bool kSlots>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
                    const TIn *__restrict__ g, const TIn *__restrict__ b, float *__restrict__ state,
-                   TIn *__restrict__ out, int N, int Hk, int Hv) {
+                   TIn *__restrict__ out, int N, int Hk, int Hv, const int32_t *__restrict__ slots,
+                   long num_slots, int *status) {
     constexpr int LPR = DK / 4;    // lanes per row
     constexpr int RPW = 32 / LPR;  // rows per warp pass
     constexpr int R = kDecodeRows;
@@ -57,13 +65,26 @@ decode_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const T
     const int grp = lane / LPR;  // row within a pass
     const int c = lane % LPR;    // float4 column
 
+    long sh = nh;  // (pool entry, value head) index of this warp's state
+    if (kSlots) {
+        const long sl = slots[n];
+        if (sl < 0 || sl >= num_slots) {
+            if (sl >= num_slots && i0 == 0 && lane == 0) flag_error(status);
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                if (c == 0) out[nh * DV + i0 + r * RPW + grp] = from_f32<TIn>(0.f);
+            return;
+        }
+        sh = sl * Hv + h;
+    }
+
     // issue the state loads first: they are the bytes that matter
     float *srow[R];
     float4 s[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int i = i0 + r * RPW + grp;
-        srow[r] = state + (nh * DV + i) * (long)DK + 4 * c;
+        srow[r] = state + (sh * DV + i) * (long)DK + 4 * c;
         s[r] = __ldcs(reinterpret_cast<const float4 *>(srow[r]));
     }
     const long kq_off = (n * Hk + hk) * (long)DK + 4 * c;
@@ -101,14 +122,15 @@ decode_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const T
 
 template <int DK, int DV, typename TIn>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
+    const auto kern = a.slots ? decode_step_kernel<DK, DV, TIn, true> : decode_step_kernel<DK, DV, TIn, false>;
     constexpr int ROWS_PER_WARP = (32 / (DK / 4)) * kDecodeRows;
     const long rows = (long)a.N * a.Hv * DV;
     const long warps = (rows + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
     const long blocks = (warps + kDecodeThreads / 32 - 1) / (kDecodeThreads / 32);
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    decode_step_kernel<DK, DV, TIn><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(
+    kern<<<(unsigned)blocks, kDecodeThreads, 0, s>>>(
         (const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, (const TIn *)a.g, (const TIn *)a.b,
-        a.state, (TIn *)a.out, a.N, a.Hk, a.Hv);
+        a.state, (TIn *)a.out, a.N, a.Hk, a.Hv, a.slots, a.num_slots, a.status);
     return cudaGetLastError();
 }
 

@@ -119,6 +119,28 @@ int gdn_decode_step(const void *q, const void *k, const void *v, const void *g, 
                                                                                    : GDN_ERR_CUDA;
 }
 
+int gdn_decode_step_slots(const void *q, const void *k, const void *v, const void *g, const void *b,
+                          float *state_pool, const int32_t *slots, void *out, int N, int num_slots,
+                          int Hk, int Hv, int dk, int dv, int dtype, void *stream) {
+    if (N < 0 || num_slots < 0) return GDN_ERR_INVALID_ARG;
+    int rc = common_checks(Hk, Hv, dk, dv, dtype);
+    if (rc != GDN_OK) return rc;
+    if (N == 0) return GDN_OK;
+    if ((long long)num_slots * Hv * dv * dk > (1LL << 40)) return GDN_ERR_INVALID_ARG;
+    if (num_slots > 0 && (!state_pool || !aligned16(state_pool))) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, b, slots, out};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    int *status = status_ptr();
+    if (!status) return GDN_ERR_CUDA;
+    gdn::DecodeArgs a{q, k, v, g, b, state_pool, out, N, Hk, Hv, dk, dv, dtype};
+    a.slots = slots;
+    a.num_slots = num_slots;
+    a.status = status;
+    return gdn::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
+                                                                                   : GDN_ERR_CUDA;
+}
+
 int gdn_prepass(const void *q, const void *k, const void *g, const void *b,
                 const int32_t *cu_seqlens, int B, int T, int Hk, int Hv, int dk, int chunk,
                 int dtype, float *rq, float *rk, float *beta, float *gcum, void *stream) {

@@ -21,6 +21,9 @@ struct DecodeArgs {
     float *state;
     void *out;
     int N, Hk, Hv, dk, dv, dtype;
+    const int32_t *slots = nullptr;  // pool entry of each sequence, or null: entry n
+    long num_slots = 0;              // pool entries (with slots)
+    int *status = nullptr;           // device status word (with slots)
 };
 
 struct PrepassArgs {

@@ -119,6 +119,34 @@ GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const v
                     void *stream);
 
 /*
+ * gdn_decode_step_slots -- one decode step for N sequences whose states sit in
+ * a pool of resident sessions.
+ *
+ * The same step as gdn_decode_step (one read and one write of each state, in
+ * place), but sequence n updates pool entry slots[n] instead of entry n, so a
+ * server can keep many sessions' states in one allocation and step any subset
+ * of them, in any order, in one launch. The pages keep each session's state on
+ * the device between tokens and move only what a token needs ("Decodage :
+ * minimiser les octets deplaces par token"); the indexing adds no state traffic.
+ *
+ *   q, k, v, g, b, out : as for gdn_decode_step ([N][...]).
+ *   state_pool : [num_slots][Hv][dv][dk] fp32, entries slots[n] updated in
+ *                place; every other entry is left untouched.
+ *   slots      : device int32 [N]. slots[n] < 0 marks a padding row: its state
+ *                is not touched and out[n] is written as zeros. Two sequences
+ *                must not name the same entry (their updates would race).
+ *                slots[n] >= num_slots is treated like padding and sets the
+ *                device status word (GDN_ERR_DEVICE_CHECK, see
+ *                gdn_get_device_status).
+ *   N, num_slots : sequences in this step (0 = no-op) and pool entries.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
+ */
+GDN_API int gdn_decode_step_slots(const void *q, const void *k, const void *v, const void *g,
+                          const void *b, float *state_pool, const int32_t *slots, void *out,
+                          int N, int num_slots, int Hk, int Hv, int dk, int dv, int dtype,
+                          void *stream);
+
+/*
  * gdn_prepass -- the per-token quantities of the block form, materialised.
  *
  * gdn_prefill computes these inside its kernels and never writes them; this

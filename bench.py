@@ -200,6 +200,7 @@ def run_ours(args, rank, world):
         sweep[str(n)] = round(us, 3)
 
     graph = decode_graph_sweep(gdn, (qd, kd, vd, gd, bd), dstate, dout, stream)
+    multi = multi_token_decode(args, gdn, flush, stream, dev)
     e2e = measure_e2e(args, gdn, pb, dec, dev, stream)
     hbm, bf16, src = peaks()
     pre_s = pre_mean / 1e3
@@ -229,7 +230,7 @@ def run_ours(args, rank, world):
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                                 "frac": round(dec_gbs / hbm, 4), "traffic": TRAFFIC["decode"],
                                 "peak_source": src},
-                   "sweep_us": sweep, "graph": graph},
+                   "sweep_us": sweep, "graph": graph, "multi_token": multi},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC["prefill"], "peak_source": src,
                      "kernel": "prefill"},
@@ -239,6 +240,34 @@ def run_ours(args, rank, world):
         "wall_s_timed_region": round(wall, 4),
     }
     return line
+
+
+def multi_token_decode(args, gdn, flush, stream, dev, N=128, T=4):
+    """N sequences x T tokens each (checking T speculated tokens) through gdn_prefill, which runs
+    them as a token scan (one pass over each state), L2 flushed before each launch."""
+    from gated_deltanet_linear_delta_gb300 import inputs
+    hbm, _, src = peaks()
+    b = inputs.make_batch(B=N, T=T, Hk=HK, Hv=HV, dk=DK, dv=DV, dtype="bf16", chunk=CHUNK, seed=0,
+                          init_state=True).to(dev)
+    out = torch.empty(b.v.shape, dtype=torch.bfloat16, device=dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(4.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gdn.gdn_prefill(b.q, b.k, b.v, b.g, b.b, b.state, b.state, out, None, B=N, T=T, chunk=CHUNK,
+                        stream=stream)
+        e1.record(stream)
+        if i >= args.warmup:
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    us = 1e3 * sum(a.elapsed_time(c) for a, c in times) / len(times)
+    nbytes = N * (2 * STATE_BYTES + T * IO_BYTES_PER_TOKEN)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"sequences": N, "tokens_per_sequence": T, "us": round(us, 3),
+            "kernel": {2: "token scan"}.get(gdn.gdn_prefill_path(N, T, HK, HV, DK, DV, CHUNK, gdn.GDN_BF16)),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "bytes": nbytes, "peak_source": src}}
 
 
 def decode_graph_sweep(gdn, qkvgb, dstate, dout, stream, G=32, reps=20):

@@ -171,7 +171,7 @@ def gdn_prepass(q, k, g, b, rq, rk, beta, gcum, cu_seqlens=None, B=None, T=None,
 
 
 def gdn_prefill_path(B, T, Hk, Hv, dk, dv, chunk, dtype) -> int:
-    """1 = tensor-core kernel, 0 = CUDA-core kernel, <0 = the status gdn_prefill would return."""
+    """2 = token scan, 1 = tensor-core kernel, 0 = CUDA-core kernel, <0 = the status gdn_prefill would return."""
     if isinstance(dtype, torch.dtype):
         dtype = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
     return library().gdn_prefill_path(B, T, Hk, Hv, dk, dv, chunk, int(dtype))

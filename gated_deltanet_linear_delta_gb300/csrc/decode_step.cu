@@ -38,6 +38,7 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeRows = 4;  // passes (rows per lane group) per warp
+constexpr int kScanMaxT = kPrefillScanMaxT;  // tokens per sequence of the token-scan kernel
 
 template <int DK, int DV, typename TIn, bool kSlots>
 __global__ void __launch_bounds__(kDecodeThreads)
@@ -120,6 +121,106 @@ decode_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const T
     }
 }
 
+// A few tokens per sequence (1 <= T <= kScanMaxT), the shape of checking a short run of
+// speculated tokens: each state row is read once from state_in (or zero), all T tokens
+// are applied in order while it sits in registers, and it is written once to state_out
+// (which may be state_in: each lane reads its pieces of a row before it writes them). The
+// T steps cost one pass over the state instead of T.
+//
+// Since every token adds two dot products per row, the row is spread over only
+// kScanLanes = 8 lanes (DK/32 float4 pieces each, interleaved so that the 8 lanes read
+// 128 contiguous bytes at a time): a 3-step shuffle reduction then serves the 4 rows of a
+// warp pass at once, where 32 lanes per row would take 5 steps for one row.
+constexpr int kScanLanes = 8;
+constexpr int kScanPasses = 2;
+
+template <int DK, int DV, typename TIn>
+__global__ void __launch_bounds__(kDecodeThreads)
+scan_tokens_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
+                   const TIn *__restrict__ g, const TIn *__restrict__ b, const float *state_in,
+                   float *state_out, TIn *__restrict__ out, int B, int T, int Hk, int Hv) {
+    constexpr int LPR = kScanLanes;
+    constexpr int CPL = DK / (4 * LPR);  // float4 pieces per lane
+    constexpr int RPW = 32 / LPR;        // rows per warp pass
+    constexpr int R = kScanPasses;
+    constexpr int ROWS_PER_WARP = RPW * R;
+    static_assert(CPL >= 1 && DV % ROWS_PER_WARP == 0, "a warp must stay within one head");
+
+    const int lane = threadIdx.x & 31;
+    const long warp = (long)blockIdx.x * (kDecodeThreads / 32) + (threadIdx.x >> 5);
+    const long row0 = warp * ROWS_PER_WARP;
+    if (row0 >= (long)B * Hv * DV) return;
+    const long nh = row0 / DV;
+    const int i0 = (int)(row0 % DV);
+    const int h = (int)(nh % Hv);
+    const long n = nh / Hv;
+    const int hk = h / (Hv / Hk);
+    const int grp = lane / LPR;  // row within a pass
+    const int c = lane % LPR;    // piece j of this lane covers columns 4 (c + LPR j) .. +3
+
+    float4 s[R][CPL];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const long off = (nh * DV + i0 + r * RPW + grp) * (long)DK;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+            s[r][j] = state_in ? __ldcs(reinterpret_cast<const float4 *>(state_in + off + 4 * (c + LPR * j)))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+        const long tok = n * T + t;
+        const long kq_off = (tok * Hk + hk) * (long)DK;
+        float4 kh[CPL], qh[CPL];
+        float pkk = 0.f, pqq = 0.f, pkq = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            kh[j] = load4(k + kq_off + 4 * (c + LPR * j));
+            qh[j] = load4(q + kq_off + 4 * (c + LPR * j));
+            pkk += dot4(kh[j], kh[j]);
+            pqq += dot4(qh[j], qh[j]);
+            pkq += dot4(kh[j], qh[j]);
+        }
+        float vi[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) vi[r] = to_f32(v[(tok * Hv + h) * DV + i0 + r * RPW + grp]);
+        const float alpha = expf(to_f32(g[tok * Hv + h]));
+        const float beta = sigmoidf_(to_f32(b[tok * Hv + h]));
+        const float rk = rsqrtf(group_sum<LPR>(pkk) + kNormEps), rq = rsqrtf(group_sum<LPR>(pqq) + kNormEps);
+        const float kq = group_sum<LPR>(pkq) * rk * rq;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            kh[j] = make_float4(kh[j].x * rk, kh[j].y * rk, kh[j].z * rk, kh[j].w * rk);
+            qh[j] = make_float4(qh[j].x * rq, qh[j].y * rq, qh[j].z * rq, qh[j].w * rq);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float psk = 0.f, psq = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                psk += dot4(s[r][j], kh[j]);
+                psq += dot4(s[r][j], qh[j]);
+            }
+            const float sk = group_sum<LPR>(psk), sq = group_sum<LPR>(psq);
+            const float u = beta * (vi[r] - alpha * sk);
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                s[r][j].x = alpha * s[r][j].x + u * kh[j].x;
+                s[r][j].y = alpha * s[r][j].y + u * kh[j].y;
+                s[r][j].z = alpha * s[r][j].z + u * kh[j].z;
+                s[r][j].w = alpha * s[r][j].w + u * kh[j].w;
+            }
+            if (c == 0) out[(tok * Hv + h) * DV + i0 + r * RPW + grp] = from_f32<TIn>(alpha * sq + u * kq);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const long off = (nh * DV + i0 + r * RPW + grp) * (long)DK;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) __stcs(reinterpret_cast<float4 *>(state_out + off + 4 * (c + LPR * j)), s[r][j]);
+    }
+}
+
 template <int DK, int DV, typename TIn>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
     const auto kern = a.slots ? decode_step_kernel<DK, DV, TIn, true> : decode_step_kernel<DK, DV, TIn, false>;
@@ -145,7 +246,40 @@ cudaError_t dispatch_dims(const DecodeArgs &a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
+template <int DK, int DV, typename TIn>
+cudaError_t launch_scan_t(const PrefillArgs &a, cudaStream_t s) {
+    constexpr int ROWS_PER_WARP = (32 / kScanLanes) * kScanPasses;
+    const long rows = (long)a.B * a.Hv * DV;
+    const long warps = (rows + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
+    const long blocks = (warps + kDecodeThreads / 32 - 1) / (kDecodeThreads / 32);
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    scan_tokens_kernel<DK, DV, TIn><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(
+        (const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, (const TIn *)a.g, (const TIn *)a.b,
+        a.state_in, a.state_out, (TIn *)a.out, a.B, a.T, a.Hk, a.Hv);
+    return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t dispatch_scan(const PrefillArgs &a, cudaStream_t s) {
+#define GDN_SCAN_CASE(DKV, DVV) \
+    if (a.dk == DKV && a.dv == DVV) return launch_scan_t<DKV, DVV, TIn>(a, s);
+    GDN_SCAN_CASE(32, 32) GDN_SCAN_CASE(32, 64) GDN_SCAN_CASE(32, 128)
+    GDN_SCAN_CASE(64, 32) GDN_SCAN_CASE(64, 64) GDN_SCAN_CASE(64, 128)
+    GDN_SCAN_CASE(128, 32) GDN_SCAN_CASE(128, 64) GDN_SCAN_CASE(128, 128)
+#undef GDN_SCAN_CASE
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+bool prefill_scan_supported(const PrefillArgs &a) {
+    return a.cu_seqlens == nullptr && a.T >= 1 && a.T <= kScanMaxT;
+}
+
+cudaError_t launch_prefill_scan(const PrefillArgs &a, cudaStream_t s) {
+    if (a.B == 0) return cudaSuccess;
+    return a.dtype == GDN_BF16 ? dispatch_scan<__nv_bfloat16>(a, s) : dispatch_scan<float>(a, s);
+}
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;

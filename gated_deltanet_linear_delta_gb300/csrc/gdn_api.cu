@@ -83,6 +83,7 @@ int gdn_prefill_path(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, in
     if (rc != GDN_OK) return rc;
     gdn::PrefillArgs a{};
     a.B = B; a.T = T; a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv; a.chunk = chunk; a.dtype = dtype;
+    if (gdn::prefill_scan_supported(a)) return 2;
     return gdn::prefill_tc_supported(a) ? 1 : 0;
 }
 
@@ -98,8 +99,9 @@ int gdn_prefill(const void *q, const void *k, const void *v, const void *g, cons
     gdn::PrefillArgs a{q, k, v, g, b, state_in, state_out, out, cu_seqlens,
                        B, T, Hk, Hv, dk, dv, chunk, dtype, status};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = gdn::prefill_tc_supported(a) ? gdn::launch_prefill_tc(a, s)
-                                                       : gdn::launch_prefill_simt(a, s);
+    const cudaError_t e = gdn::prefill_scan_supported(a) ? gdn::launch_prefill_scan(a, s)
+                          : gdn::prefill_tc_supported(a) ? gdn::launch_prefill_tc(a, s)
+                                                         : gdn::launch_prefill_simt(a, s);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -6,6 +6,9 @@
 
 namespace gdn {
 
+// gdn_prefill runs sequences of at most this many tokens (no cu_seqlens) as a token scan
+constexpr int kPrefillScanMaxT = 8;
+
 struct PrefillArgs {
     const void *q, *k, *v, *g, *b;
     const float *state_in;
@@ -39,5 +42,7 @@ cudaError_t launch_prepass(const PrepassArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);
+bool prefill_scan_supported(const PrefillArgs &a);
+cudaError_t launch_prefill_scan(const PrefillArgs &a, cudaStream_t s);
 
 }  // namespace gdn

@@ -92,6 +92,11 @@ typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
  *                   total packed tokens (cu_seqlens given).
  *   Hk, Hv, dk, dv: head counts and head dimensions; dk, dv in {32, 64, 128}.
  *   chunk         : block length, one of 16, 32, 64.
+ * Sequences of at most 8 tokens each (cu_seqlens NULL, T <= 8: a few tokens
+ * per sequence, e.g. checking a run of speculated tokens) are evaluated as a
+ * token scan instead: every state row is read once, takes the T updates in
+ * order in registers, and is written once, so T steps cost one pass over the
+ * state. The result is the same function (only the rounding order differs).
  * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
  */
 GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void *g, const void *b,
@@ -163,7 +168,8 @@ GDN_API int gdn_prepass(const void *q, const void *k, const void *g, const void 
 
 /*
  * gdn_prefill_path -- which kernel gdn_prefill would launch for these sizes:
- * 1 = tensor-core block kernel (tcgen05/TMEM/TMA), 0 = CUDA-core block kernel,
+ * 2 = token scan (T <= 8 tokens per sequence, cu_seqlens NULL), 1 = tensor-core
+ * block kernel (tcgen05/TMEM/TMA), 0 = CUDA-core block kernel,
  * negative = the gdn_status gdn_prefill would return. Host-only, no device work.
  */
 GDN_API int gdn_prefill_path(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype);

@@ -99,8 +99,34 @@ def test_decode_zero_batch_is_a_noop(lib):
     assert decode(lib, N=0) == 0
 
 
+def decode_slots(lib, **kw):
+    args = dict(q=A, k=A, v=A, g=A, b=A, pool=A, slots=A, out=A, N=4, S=8, Hk=2, Hv=4, dk=128, dv=128,
+                dtype=0)
+    args.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.gdn_decode_step_slots(p(args["q"]), p(args["k"]), p(args["v"]), p(args["g"]), p(args["b"]),
+                                     p(args["pool"]), p(args["slots"]), p(args["out"]), args["N"], args["S"],
+                                     args["Hk"], args["Hv"], args["dk"], args["dv"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=16), -2), (dict(dtype=2), -2), (dict(Hk=3, Hv=4), -1), (dict(N=-1), -1), (dict(S=-1), -1),
+    (dict(slots=None), -1), (dict(slots=A + 4), -1), (dict(pool=None), -1), (dict(pool=A + 8), -1),
+    (dict(out=None), -1),
+])
+def test_decode_slots_rejects(lib, kw, code):
+    assert decode_slots(lib, **kw) == code
+
+
+def test_decode_slots_zero_batch_is_a_noop(lib):
+    assert decode_slots(lib, N=0) == 0
+
+
 def test_prefill_path_selection(lib):
     import gated_deltanet_linear_delta_gb300 as gdn
+    for T in (1, 4, 8):  # a few tokens per sequence: token scan
+        assert gdn.gdn_prefill_path(16, T, 16, 32, 128, 128, 64, 0) == 2
+    assert gdn.gdn_prefill_path(16, 9, 16, 32, 128, 128, 64, 0) == 1
     assert gdn.gdn_prefill_path(1, 64, 2, 4, 48, 128, 64, 0) == -2
     assert gdn.gdn_prefill_path(1, 64, 2, 4, 32, 32, 16, 1) == 0  # tiny fp32: CUDA-core kernel
     assert gdn.gdn_prefill_path(1, 4096, 16, 32, 128, 128, 64, 0) in (0, 1)

@@ -73,4 +73,27 @@ __device__ __forceinline__ bool seq_bounds(const int32_t *cu, int n, int B, long
     return true;
 }
 
+// Packed sequences are taken longest first: CTA row y works on the sequence of rank y, where
+// sequence m's rank counts the sequences longer than it (ties: lower index first). With
+// sequences of mixed lengths this starts the longest chains of blocks first, so that they do
+// not finish alone at the end of the launch. Rank is a permutation even when cu_seqlens is
+// inconsistent (such sequences are still reported by seq_bounds). Every thread of the CTA calls
+// this (it synchronises the CTA); above kRankMaxSeqs sequences row y keeps sequence y.
+constexpr int kRankMaxSeqs = 128;
+__device__ __forceinline__ int longest_first(const int32_t *cu, int B, int y) {
+    if (cu == nullptr || B > kRankMaxSeqs) return y;
+    __shared__ int s_len[kRankMaxSeqs];
+    __shared__ int s_pick;
+    for (int m = threadIdx.x; m < B; m += blockDim.x) s_len[m] = cu[m + 1] - cu[m];
+    __syncthreads();
+    for (int m = threadIdx.x; m < B; m += blockDim.x) {
+        const int lm = s_len[m];
+        int rank = 0;
+        for (int o = 0; o < B; ++o) rank += (s_len[o] > lm) || (s_len[o] == lm && o < m);
+        if (rank == y) s_pick = m;
+    }
+    __syncthreads();
+    return s_pick;
+}
+
 }  // namespace gdn

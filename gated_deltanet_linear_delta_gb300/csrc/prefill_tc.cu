@@ -321,7 +321,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = p.P, F = p.F, NP = P - F;
     const int rank = P > 1 ? (int)cluster_ctarank() : 0;
-    const int h = blockIdx.x / P, n = blockIdx.y;
+    const int h = blockIdx.x / P, n = longest_first(p.cu, p.B, blockIdx.y);
     const int hk = h / (p.Hv / p.Hk);
     long bos, eos;
     if (!seq_bounds(p.cu, n, p.B, p.cu ? p.Ttot : p.T, &bos, &eos, p.status)) return;

@@ -46,7 +46,7 @@ PREFILL_FLOPS_PER_TOKEN = HV * (5 * 2 * CHUNK * DK + 3 * 2 * DK * DV)  # chunk G
 DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + IO_BYTES_PER_TOKEN
 # DRAM bytes per launch from the committed ncu captures (profiles/); None once a kernel
 # has changed since its capture.
-TRAFFIC = {"prefill": None, "decode": 480.2e6}  # prefill: kernel changed since its capture
+TRAFFIC = {"prefill": 76.18e6, "decode": 480.2e6, "scan": 486.9e6}
 
 
 def peaks():
@@ -200,6 +200,7 @@ def run_ours(args, rank, world):
         sweep[str(n)] = round(us, 3)
 
     graph = decode_graph_sweep(gdn, (qd, kd, vd, gd, bd), dstate, dout, stream)
+    other = other_prefill_workloads(args, gdn, flush, stream, dev)
     multi = multi_token_decode(args, gdn, flush, stream, dev)
     e2e = measure_e2e(args, gdn, pb, dec, dev, stream)
     hbm, bf16, src = peaks()
@@ -231,6 +232,7 @@ def run_ours(args, rank, world):
                                 "frac": round(dec_gbs / hbm, 4), "traffic": TRAFFIC["decode"],
                                 "peak_source": src},
                    "sweep_us": sweep, "graph": graph, "multi_token": multi},
+        "other_workloads": other,
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC["prefill"], "peak_source": src,
                      "kernel": "prefill"},
@@ -240,6 +242,43 @@ def run_ours(args, rank, world):
         "wall_s_timed_region": round(wall, 4),
     }
     return line
+
+
+def other_prefill_workloads(args, gdn, flush, stream, dev, reps=5):
+    """The other prefill workloads (reported, not the headline): one 32768-token sequence with a
+    seeded initial state, and 16 packed sequences of lengths U{256..16384} with their own states
+    (131072 tokens with --all-workloads). L2 flushed before each launch; median of `reps`."""
+    from gated_deltanet_linear_delta_gb300 import inputs
+    hbm, bf16, src = peaks()
+    cases = [("T=32768, seeded state", lambda: inputs.prefill_long(T=32768)),
+             ("varlen 16 seqs U{256..16384}, seeded states", inputs.prefill_varlen)]
+    if args.all_workloads:
+        cases.append(("T=131072, seeded state", lambda: inputs.prefill_long(T=131072)))
+    res = {}
+    for name, make in cases:
+        b = make().to(dev)
+        ntok = int(b.q.shape[0])
+        out = torch.empty(b.v.shape, dtype=torch.bfloat16, device=dev)
+        so = torch.empty(b.B, HV, DV, DK, device=dev)
+        ev = []
+        for i in range(2 + reps):
+            flush.fill_(5.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gdn.gdn_prefill(b.q, b.k, b.v, b.g, b.b, b.state, so, out, b.cu_seqlens, B=b.B,
+                            T=None if b.cu_seqlens is not None else b.T, chunk=CHUNK, stream=stream)
+            e1.record(stream)
+            if i >= 2:
+                ev.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(c) for a, c in ev)[len(ev) // 2]
+        nbytes = ntok * IO_BYTES_PER_TOKEN + 2 * b.B * STATE_BYTES
+        roof = max(nbytes / (hbm * 1e9), ntok * PREFILL_FLOPS_PER_TOKEN / (bf16 * 1e12))
+        res[name] = {"tokens": ntok, "ms": round(ms, 4), "Mtok_s": round(ntok / ms / 1e3, 3),
+                     "GB_s": round(nbytes / ms / 1e6, 1), "roofline_ms": round(roof * 1e3, 4),
+                     "frac_of_roofline": round(roof * 1e3 / ms, 4)}
+        del b, out, so
+    return res
 
 
 def multi_token_decode(args, gdn, flush, stream, dev, N=128, T=4):
@@ -267,7 +306,8 @@ def multi_token_decode(args, gdn, flush, stream, dev, N=128, T=4):
     return {"sequences": N, "tokens_per_sequence": T, "us": round(us, 3),
             "kernel": {2: "token scan"}.get(gdn.gdn_prefill_path(N, T, HK, HV, DK, DV, CHUNK, gdn.GDN_BF16)),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4), "bytes": nbytes, "peak_source": src}}
+                         "frac": round(gbs / hbm, 4), "bytes": nbytes, "traffic": TRAFFIC["scan"],
+                         "peak_source": src}}
 
 
 def decode_graph_sweep(gdn, qkvgb, dstate, dout, stream, G=32, reps=20):
@@ -363,6 +403,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-workloads", action="store_true", help="also time the 131072-token prompt")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -118,6 +118,19 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum over all ranks (the slowest replica sets the job's time)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world, units_per_rank, seconds):
+    """Whole-job rate of `world` replicas that each process `units_per_rank` units, timed by
+    the slowest: every rank runs its own copy of the workload (weak scaling, no exchange)."""
+    return world * units_per_rank / seconds
+
+
 def make_inputs(dev):
     from gated_deltanet_linear_delta_gb300 import inputs
     pb = inputs.prefill_4k(seed=0)
@@ -179,9 +192,7 @@ def run_ours(args, rank, world):
     pre_mean, dec_mean = sum(pre_ms) / len(pre_ms), sum(dec_ms) / len(dec_ms)
     step_ms = pre_mean + dec_mean
     if world > 1:
-        t = torch.tensor([pre_mean, dec_mean, step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        pre_mean, dec_mean, step_ms = (float(x) for x in t)
+        pre_mean, dec_mean, step_ms = max_over_ranks([pre_mean, dec_mean, step_ms], dev)
 
     # decode batch sweep (same kernel, smaller batches), L2 flushed before each launch
     sweep = {}
@@ -212,7 +223,7 @@ def run_ours(args, rank, world):
     dec_gbs = dec_bytes / (dec_mean / 1e3) / 1e9
     path = gdn.gdn_prefill_path(1, T_PREFILL, HK, HV, DK, DV, CHUNK, gdn.GDN_BF16)
     clocks = clk.summary()
-    value = world * T_PREFILL / pre_s / 1e6
+    value = job_throughput(world, T_PREFILL, pre_s) / 1e6
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "Mtok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),

@@ -20,7 +20,7 @@ import torch
 
 from . import _build
 
-__all__ = ["GDNError", "gdn_prefill", "gdn_decode_step", "gdn_decode_step_slots", "gdn_prepass", "gdn_prefill_path",
+__all__ = ["GDNError", "gdn_prefill", "gdn_prefill_from_host", "gdn_decode_step", "gdn_decode_step_slots", "gdn_prepass", "gdn_prefill_path",
            "gdn_get_device_status", "gdn_status_string", "library", "library_path",
            "GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
            "GDN_ERR_DEVICE_CHECK", "GDN_BF16", "GDN_F32"]
@@ -58,6 +58,8 @@ def library() -> ctypes.CDLL:
             lib.gdn_prefill.restype = _I
             lib.gdn_decode_step.argtypes = [_P] * 7 + [_I] * 6 + [_P]
             lib.gdn_decode_step.restype = _I
+            lib.gdn_prefill_from_host.argtypes = [_P] * 15 + [_I] * 8 + [_P]
+            lib.gdn_prefill_from_host.restype = _I
             lib.gdn_decode_step_slots.argtypes = [_P] * 8 + [_I] * 7 + [_P]
             lib.gdn_decode_step_slots.restype = _I
             lib.gdn_prepass.argtypes = [_P] * 5 + [_I] * 7 + [_P] * 4 + [_P]
@@ -126,6 +128,32 @@ def gdn_prefill(q, k, v, g, b, state_in, state_out, out, cu_seqlens=None, B=None
                                _ptr(state_out), _ptr(out), _ptr(cu_seqlens), B, T, Hk, Hv, dk, dv,
                                chunk, dt, _stream(stream))
     _check(rc, "gdn_prefill")
+
+
+def _host_ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("host arrays must be contiguous CPU tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def gdn_prefill_from_host(q, k, v, g, b, state_in, state_out, out, dev, chunk=64, fragment=1024,
+                          stream=None) -> None:
+    """Prefill of one sequence from host tensors (pinned for overlap): q..b, state_in (or None),
+    state_out and out are CPU tensors; `dev` holds the device buffers of the same shapes (keys
+    q, k, v, g, b, out, state). Copies overlap the computation fragment by fragment."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    for t in (state_in, state_out):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("states are fp32")
+    rc = library().gdn_prefill_from_host(
+        _host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(g), _host_ptr(b), _host_ptr(state_in),
+        _host_ptr(state_out), _host_ptr(out), _ptr(dev["q"]), _ptr(dev["k"]), _ptr(dev["v"]), _ptr(dev["g"]),
+        _ptr(dev["b"]), _ptr(dev["state"]), _ptr(dev["out"]), T, Hk, Hv, dk, dv, chunk, _dtype_code(q),
+        fragment, _stream(stream))
+    _check(rc, "gdn_prefill_from_host")
 
 
 def gdn_decode_step(q, k, v, g, b, state, out, stream=None) -> None:

@@ -152,6 +152,42 @@ GDN_API int gdn_decode_step_slots(const void *q, const void *k, const void *v, c
                           void *stream);
 
 /*
+ * gdn_prefill_from_host -- gdn_prefill of ONE sequence whose inputs and outputs are in
+ * host memory, with the copies overlapped with the computation.
+ *
+ * The state is carried from one prompt fragment to the next with an unchanged result
+ * ("Limiter la memoire temporaire grace au decoupage des prompts"), so the prompt is
+ * processed in fragments of `fragment` tokens: while fragment f is computed on `stream`,
+ * fragment f+1's inputs are copied in and fragment f-1's outputs copied out on two streams
+ * the library keeps per device. With every fragment longer than 8 tokens the result is
+ * bit-identical to gdn_prefill on the whole prompt (the same blocks, the state carried in
+ * fp32 through device memory).
+ *
+ *   q_h, k_h, v_h, g_h, b_h, out_h : host arrays, layouts as for gdn_prefill with B = 1
+ *                   (page-locked memory lets the copies overlap; pageable memory works but
+ *                   the copies then do not overlap).
+ *   state_in_h    : host [Hv][dv][dk] fp32 initial state, or NULL for zeros.
+ *   state_out_h   : host [Hv][dv][dk] fp32 final state (may equal state_in_h).
+ *   q_d .. out_d, state_d : caller-owned DEVICE buffers of the full prompt's sizes (and
+ *                   one state); the library copies into and computes in them. They must
+ *                   not be in use by other work while the call's work is in flight.
+ *   T             : tokens of the prompt (0: the state passes through).
+ *   fragment      : tokens per fragment, a positive multiple of `chunk`; at most 256
+ *                   fragments.
+ *   Other arguments as for gdn_prefill.
+ * The call is asynchronous on `stream`: its copies start after the work already queued on
+ * `stream`, and work queued on `stream` afterwards starts after the last copy (so
+ * synchronising `stream` means the host outputs are written). Calls from several host
+ * threads on one device are serialised while they queue work.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
+ */
+GDN_API int gdn_prefill_from_host(const void *q_h, const void *k_h, const void *v_h, const void *g_h,
+                          const void *b_h, const float *state_in_h, float *state_out_h, void *out_h,
+                          void *q_d, void *k_d, void *v_d, void *g_d, void *b_d, float *state_d,
+                          void *out_d, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype,
+                          int fragment, void *stream);
+
+/*
  * gdn_prepass -- the per-token quantities of the block form, materialised.
  *
  * gdn_prefill computes these inside its kernels and never writes them; this

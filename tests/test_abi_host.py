@@ -122,6 +122,22 @@ def test_decode_slots_zero_batch_is_a_noop(lib):
     assert decode_slots(lib, N=0) == 0
 
 
+def from_host(lib, **kw):
+    args = dict(T=256, fragment=128, chunk=64, dk=128, sd=A, so=A)
+    args.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.gdn_prefill_from_host(*([p(A)] * 5), None, p(args["so"]), p(A), *([p(A)] * 5), p(args["sd"]), p(A),
+                                     args["T"], 2, 4, args["dk"], 128, args["chunk"], 0, args["fragment"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(fragment=0), -1), (dict(fragment=100), -1), (dict(T=-1), -1), (dict(so=None), -1),
+    (dict(sd=None), -1), (dict(T=300 * 128), -1), (dict(dk=48), -2), (dict(chunk=48, fragment=96), -2),
+])
+def test_prefill_from_host_rejects(lib, kw, code):
+    assert from_host(lib, **kw) == code
+
+
 def test_prefill_path_selection(lib):
     import gated_deltanet_linear_delta_gb300 as gdn
     for T in (1, 4, 8):  # a few tokens per sequence: token scan

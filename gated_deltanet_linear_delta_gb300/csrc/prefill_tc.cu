@@ -397,10 +397,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             issue_tma((int)(bos + (long)first * C));
             tma_issued = 1;
         }
-        float g_nx = 0.f, b_nx = 0.f;  // gates of the next block, fetched one block ahead
+        // gates of the next block, fetched one block ahead and kept in bf16 until used, so that
+        // the load's latency overlaps a whole block of work
+        __nv_bfloat16 g_nx = __float2bfloat16(0.f), b_nx = __float2bfloat16(0.f);
         if (pt < C && first < nchunks && bos + (long)first * C + pt < eos) {
-            g_nx = to_f32(p.g[(bos + (long)first * C + pt) * p.Hv + h]);
-            b_nx = to_f32(p.b[(bos + (long)first * C + pt) * p.Hv + h]);
+            g_nx = p.g[(bos + (long)first * C + pt) * p.Hv + h];
+            b_nx = p.b[(bos + (long)first * C + pt) * p.Hv + h];
         }
         int jb = 0;  // this CTA's job count
         for (int k = first; k < nchunks; k += NP, ++jb) {
@@ -415,12 +417,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float *sT = reinterpret_cast<float *>(st + ST_TB);
             float *sX = reinterpret_cast<float *>(sm + TW);
             if (pt < C) {
-                ps[PS_G + pt] = pt < L ? g_nx : 0.f;
-                ps[PS_BETA + pt] = pt < L ? sigmoidf_(b_nx) : 0.f;
+                ps[PS_G + pt] = pt < L ? __bfloat162float(g_nx) : 0.f;
+                ps[PS_BETA + pt] = pt < L ? sigmoidf_(__bfloat162float(b_nx)) : 0.f;
                 const long cn = c0 + (long)NP * C + pt;
                 if (k + NP < nchunks && cn < eos) {
-                    g_nx = to_f32(p.g[cn * p.Hv + h]);
-                    b_nx = to_f32(p.b[cn * p.Hv + h]);
+                    g_nx = p.g[cn * p.Hv + h];
+                    b_nx = p.b[cn * p.Hv + h];
                 }
             }
             if (!mbar_wait(bar_tma, jb & 1, kWaitBudget)) ab = true;  // every reader of the tiles waits (asleep)

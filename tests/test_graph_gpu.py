@@ -89,3 +89,18 @@ def test_graph_of_prefill_matches_eager():
     torch.cuda.synchronize()
     assert gdn.gdn_get_device_status() == gdn.GDN_OK
     assert torch.equal(outs[0], outs[1]) and torch.equal(sts[0], sts[1])
+
+
+def test_graph_of_few_token_prefill_matches_eager():
+    """The few-token (token-scan) path, in place, captured and replayed."""
+    b = inputs.make_batch(B=16, T=4, Hk=16, Hv=32, dk=128, dv=128, dtype="bf16", chunk=64, seed=36,
+                          init_state=True)
+    d = b.to(DEV)
+    out_g, out_e = torch.empty_like(d.v), torch.empty_like(d.v)
+    st_g, st_e = d.state.clone(), d.state.clone()
+    graph = _capture(lambda: gdn.gdn_prefill(d.q, d.k, d.v, d.g, d.b, st_g, st_g, out_g, None, B=16, T=4))
+    st_g.copy_(d.state)
+    graph.replay()
+    gdn.gdn_prefill(d.q, d.k, d.v, d.g, d.b, st_e, st_e, out_e, None, B=16, T=4)
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, out_e) and torch.equal(st_g, st_e)

@@ -67,3 +67,22 @@ def test_from_host_empty_prompt_passes_state():
     gdn.gdn_prefill_from_host(e(b.q), e(b.k), e(b.v), e(b.g), e(b.b), sin, sout, e(b.v), dev, fragment=64)
     torch.cuda.current_stream().synchronize()
     assert torch.equal(sout, b.state[0])
+
+
+def test_from_host_pageable_memory_and_short_last_fragment():
+    """Pageable host tensors work too (the copies then do not overlap), and a last fragment of a
+    few tokens goes through the token scan: equal to the device call within the oracle's bars."""
+    b = inputs.make_batch(B=1, T=64 * 5 + 3, Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", chunk=64, seed=72,
+                          init_state=True)
+    host = {n: getattr(b, n).clone() for n in ("q", "k", "v", "g", "b")}  # pageable
+    sout = torch.empty(4, 128, 128)
+    out = torch.empty(b.v.shape, dtype=b.v.dtype)
+    dev = {n: torch.empty_like(t, device=DEV) for n, t in host.items()}
+    dev["out"] = torch.empty(b.v.shape, dtype=b.v.dtype, device=DEV)
+    dev["state"] = torch.empty(4, 128, 128, device=DEV)
+    gdn.gdn_prefill_from_host(host["q"], host["k"], host["v"], host["g"], host["b"], b.state[0].clone(), sout, out,
+                              dev, chunk=64, fragment=64)
+    torch.cuda.current_stream().synchronize()
+    ro, rs = oracle.gdn_sequential(b.q, b.k, b.v, b.g, b.b, b.state, None, B=1, threads=threads())
+    assert prefill_out_err(out, ro) <= PREFILL_OUT_TOL
+    assert state_err(sout, rs[0]) <= STATE_TOL

@@ -135,7 +135,7 @@ constexpr int kScanLanes = 8;
 constexpr int kScanPasses = 2;
 
 template <int DK, int DV, typename TIn>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 3)
 scan_tokens_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
                    const TIn *__restrict__ g, const TIn *__restrict__ b, const float *state_in,
                    float *state_out, TIn *__restrict__ out, int B, int T, int Hk, int Hv) {

@@ -381,13 +381,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float *ps = reinterpret_cast<float *>(sm + PSC);
         float *red = ps + PS_RED;
         uint32_t ph_prep = 0;
+        // (a helper of a state-only CTA needs no V: the state CTA multiplies the raw V tile itself)
         auto issue_tma = [&](int c_tok) {
-            mbar_expect_tx(bar_tma, 6 * 8192);
+            mbar_expect_tx(bar_tma, (send_raw ? 4 : 6) * 8192);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
                 tma_load_3d(sm + RAW + kb * 16384, &tm_k, kb * 64, hk, c_tok, bar_tma);
                 tma_load_3d(sm + RAW + kb * 16384 + 8192, &tm_q, kb * 64, hk, c_tok, bar_tma);
-                tma_load_3d(sm + RAW + 32768 + kb * 8192, &tm_v, kb * 64, h, c_tok, bar_tma);
+                if (!send_raw) tma_load_3d(sm + RAW + 32768 + kb * 8192, &tm_v, kb * 64, h, c_tok, bar_tma);
             }
         };
         if (pt == 0 && first < nchunks) {
@@ -454,6 +455,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int vt = pt >> 2, vq = (pt & 3) * 4;  // V: row vt, chunks vq..vq+3 of 16
             uint4 rawv[4];
             float vmax = 0.f;
+            if (!send_raw) {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int c = vq + cc;
@@ -462,6 +464,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 unpack8(rawv[cc], x);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) vmax = fmaxf(vmax, fabsf(x[e]));
+            }
             }
             vmax = warp_max(vt < L ? vmax : 0.f);
             if (lane == 0) red[RED_V * 32 + warp * 4] = vmax;

@@ -212,6 +212,7 @@ def run_ours(args, rank, world):
 
     graph = decode_graph_sweep(gdn, (qd, kd, vd, gd, bd), dstate, dout, stream)
     other = other_prefill_workloads(args, gdn, flush, stream, dev)
+    copy_ref = copy_reference(args, flush, stream, dev)
     multi = multi_token_decode(args, gdn, flush, stream, dev)
     e2e = measure_e2e(args, gdn, pb, dec, dev, stream)
     hbm, bf16, src = peaks()
@@ -242,7 +243,7 @@ def run_ours(args, rank, world):
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                                 "frac": round(dec_gbs / hbm, 4), "traffic": TRAFFIC["decode"],
                                 "peak_source": src},
-                   "sweep_us": sweep, "graph": graph, "multi_token": multi},
+                   "sweep_us": sweep, "graph": graph, "multi_token": multi, "copy_reference": copy_ref},
         "other_workloads": other,
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC["prefill"], "peak_source": src,
@@ -253,6 +254,28 @@ def run_ours(args, rank, world):
         "wall_s_timed_region": round(wall, 4),
     }
     return line
+
+
+def copy_reference(args, flush, stream, dev):
+    """The decode step with its arithmetic removed: a device copy that reads and writes the same
+    state bytes (128 sequences x 32 heads x 64 KiB), L2 flushed, CUDA events. This is what the
+    decode kernel's memory traffic can reach on this GPU, measured in the same run."""
+    src = torch.empty(N_DECODE * STATE_BYTES // 4, dtype=torch.float32, device=dev).normal_()
+    dst = torch.empty_like(src)
+    ev = []
+    for i in range(args.warmup + min(args.steps, 50)):
+        flush.fill_(6.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dst.copy_(src)
+        e1.record(stream)
+        if i >= args.warmup:
+            ev.append((e0, e1))
+    torch.cuda.synchronize()
+    us = 1e3 * sorted(a.elapsed_time(c) for a, c in ev)[len(ev) // 2]
+    nbytes = 2 * N_DECODE * STATE_BYTES
+    return {"us": round(us, 3), "GB_s": round(nbytes / us / 1e3, 1), "bytes": nbytes,
+            "what": "torch copy of the decode state bytes (read + write), L2 flushed"}
 
 
 def other_prefill_workloads(args, gdn, flush, stream, dev, reps=5):
@@ -404,9 +427,33 @@ def cpu_baseline_sample(threads=None, tokens=T_PREFILL, steps=1, warmup=0):
         if i >= warmup:
             times.append(time.perf_counter() - t0)
     dt = sum(times) / len(times)
+    # one thread on a quarter of the sample (the per-core rate, next to the multi-core one)
+    t1_tokens = max(tokens // 4, 1)
+    s1 = slice(0, t1_tokens)
+    t0 = time.perf_counter()
+    oracle.gdn_sequential(*[x[s1] for x in args], None, None, B=1, threads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": round(tokens / dt / 1e6, 6), "unit": "Mtok/s", "cores": min(threads, HV), "kind": "oracle",
             "sample": f"{tokens} tokens of the 4096-token prompt, all 32 value heads, fp64 token scan",
-            "seconds_per_pass": round(dt, 3)}
+            "seconds_per_pass": round(dt, 3), "cpu_model": cpu_model(),
+            "single_thread": {"value": round(t1_tokens / dt1 / 1e6, 6), "unit": "Mtok/s",
+                              "sample": f"{t1_tokens} tokens, all 32 value heads, one thread"}}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
 
 
 def main():

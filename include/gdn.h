@@ -203,9 +203,10 @@ GDN_API int gdn_prepass(const void *q, const void *k, const void *g, const void 
                 int dtype, float *rq, float *rk, float *beta, float *gcum, void *stream);
 
 /*
- * gdn_prefill_path -- which kernel gdn_prefill would launch for these sizes:
- * 2 = token scan (T <= 8 tokens per sequence, cu_seqlens NULL), 1 = tensor-core
- * block kernel (tcgen05/TMEM/TMA), 0 = CUDA-core block kernel,
+ * gdn_prefill_path -- which kernel gdn_prefill would launch for these sizes with
+ * cu_seqlens NULL: 2 = token scan (T <= 8 tokens per sequence), 1 = tensor-core
+ * block kernel (tcgen05/TMEM/TMA), 0 = CUDA-core block kernel (with cu_seqlens
+ * given, T is the packed total and a 2 stands for the block kernel 1 or 0 would name),
  * negative = the gdn_status gdn_prefill would return. Host-only, no device work.
  */
 GDN_API int gdn_prefill_path(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype);

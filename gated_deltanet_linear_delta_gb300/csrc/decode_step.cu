@@ -127,6 +127,9 @@ decode_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const T
 // (which may be state_in: each lane reads its pieces of a row before it writes them). The
 // T steps cost one pass over the state instead of T.
 //
+// The key and query norms of a token are the same for every row of a head, so each CTA
+// computes them once (one warp per token) into shared memory before the scan.
+//
 // Since every token adds two dot products per row, the row is spread over only
 // kScanLanes = 8 lanes (DK/32 float4 pieces each, interleaved so that the 8 lanes read
 // 128 contiguous bytes at a time): a 3-step shuffle reduction then serves the 4 rows of a
@@ -146,10 +149,14 @@ scan_tokens_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const T
     constexpr int ROWS_PER_WARP = RPW * R;
     static_assert(CPL >= 1 && DV % ROWS_PER_WARP == 0, "a warp must stay within one head");
 
-    const int lane = threadIdx.x & 31;
-    const long warp = (long)blockIdx.x * (kDecodeThreads / 32) + (threadIdx.x >> 5);
+    // warps of this CTA that share a head (a CTA holds one head, or two when DV = 32)
+    constexpr int GW = DV / ROWS_PER_WARP < kDecodeThreads / 32 ? DV / ROWS_PER_WARP : kDecodeThreads / 32;
+    __shared__ float s_nrm[kDecodeThreads / 32 / GW][kScanMaxT][3];  // per head and token: rk, rq, k.q
+
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long warp = (long)blockIdx.x * (kDecodeThreads / 32) + wib;
     const long row0 = warp * ROWS_PER_WARP;
-    if (row0 >= (long)B * Hv * DV) return;
+    const bool valid = row0 < (long)B * Hv * DV;
     const long nh = row0 / DV;
     const int i0 = (int)(row0 % DV);
     const int h = (int)(nh % Hv);
@@ -159,35 +166,55 @@ scan_tokens_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const T
     const int c = lane % LPR;    // piece j of this lane covers columns 4 (c + LPR j) .. +3
 
     float4 s[R][CPL];
+    if (valid) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const long off = (nh * DV + i0 + r * RPW + grp) * (long)DK;
+        for (int r = 0; r < R; ++r) {
+            const long off = (nh * DV + i0 + r * RPW + grp) * (long)DK;
 #pragma unroll
-        for (int j = 0; j < CPL; ++j)
-            s[r][j] = state_in ? __ldcs(reinterpret_cast<const float4 *>(state_in + off + 4 * (c + LPR * j)))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < CPL; ++j)
+                s[r][j] = state_in ? __ldcs(reinterpret_cast<const float4 *>(state_in + off + 4 * (c + LPR * j)))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // the norms of this head's tokens, once per CTA: warp w of the head takes tokens w, w + GW, ...
+        for (int t = wib % GW; t < T; t += GW) {
+            const long kq_off = ((n * T + t) * Hk + hk) * (long)DK;
+            float pkk = 0.f, pqq = 0.f, pkq = 0.f;
+#pragma unroll
+            for (int j = 0; j < DK / 32; ++j) {
+                const float kx = to_f32(k[kq_off + lane + 32 * j]), qx = to_f32(q[kq_off + lane + 32 * j]);
+                pkk += kx * kx;
+                pqq += qx * qx;
+                pkq += kx * qx;
+            }
+            pkk = warp_sum(pkk);
+            pqq = warp_sum(pqq);
+            pkq = warp_sum(pkq);
+            if (lane == 0) {
+                s_nrm[wib / GW][t][0] = rsqrtf(pkk + kNormEps);
+                s_nrm[wib / GW][t][1] = rsqrtf(pqq + kNormEps);
+                s_nrm[wib / GW][t][2] = pkq;
+            }
+        }
     }
+    __syncthreads();
+    if (!valid) return;
 #pragma unroll 1
     for (int t = 0; t < T; ++t) {
         const long tok = n * T + t;
         const long kq_off = (tok * Hk + hk) * (long)DK;
         float4 kh[CPL], qh[CPL];
-        float pkk = 0.f, pqq = 0.f, pkq = 0.f;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             kh[j] = load4(k + kq_off + 4 * (c + LPR * j));
             qh[j] = load4(q + kq_off + 4 * (c + LPR * j));
-            pkk += dot4(kh[j], kh[j]);
-            pqq += dot4(qh[j], qh[j]);
-            pkq += dot4(kh[j], qh[j]);
         }
         float vi[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) vi[r] = to_f32(v[(tok * Hv + h) * DV + i0 + r * RPW + grp]);
         const float alpha = expf(to_f32(g[tok * Hv + h]));
         const float beta = sigmoidf_(to_f32(b[tok * Hv + h]));
-        const float rk = rsqrtf(group_sum<LPR>(pkk) + kNormEps), rq = rsqrtf(group_sum<LPR>(pqq) + kNormEps);
-        const float kq = group_sum<LPR>(pkq) * rk * rq;
+        const float rk = s_nrm[wib / GW][t][0], rq = s_nrm[wib / GW][t][1];
+        const float kq = s_nrm[wib / GW][t][2] * rk * rq;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             kh[j] = make_float4(kh[j].x * rk, kh[j].y * rk, kh[j].z * rk, kh[j].w * rk);

@@ -311,8 +311,47 @@ def other_prefill_workloads(args, gdn, flush, stream, dev, reps=5):
         res[name] = {"tokens": ntok, "ms": round(ms, 4), "Mtok_s": round(ntok / ms / 1e3, 3),
                      "GB_s": round(nbytes / ms / 1e6, 1), "roofline_ms": round(roof * 1e3, 4),
                      "frac_of_roofline": round(roof * 1e3 / ms, 4)}
+        if b.cu_seqlens is not None:  # then 128 decode steps on the sequences' final states
+            res[name]["then_128_decode_steps"] = decode_after_prefill(gdn, so, stream, dev, steps=128)
         del b, out, so
     return res
+
+
+def decode_after_prefill(gdn, states, stream, dev, steps=128):
+    """`steps` decode steps on the states a prefill left (in place), captured once in a CUDA graph
+    and replayed; fresh seeded token inputs per step; us per step and the rate of the
+    bytes moved (each step reads and writes every state once)."""
+    from gated_deltanet_linear_delta_gb300 import inputs
+    n = states.shape[0]
+    q, k, v, g, b, _ = inputs.make_decode_inputs(n, seed=7, steps=steps)
+    q, k, v, g, b = (x.to(dev) for x in (q, k, v, g, b))
+    out = torch.empty(steps, n, HV, DV, dtype=torch.bfloat16, device=dev)
+    st = states.clone()
+
+    def run():
+        for t in range(steps):
+            gdn.gdn_decode_step(q[t], k[t], v[t], g[t], b[t], st, out[t])
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        run()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        graph.replay()
+        ev[0].record(stream)
+        for _ in range(3):
+            graph.replay()
+        ev[1].record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * ev[0].elapsed_time(ev[1]) / (3 * steps)
+    nbytes = n * DECODE_BYTES_PER_SEQ
+    return {"sequences": n, "us_per_step": round(us, 3), "GB_s": round(nbytes / us / 1e3, 1),
+            "l2": f"warm: the {n} states ({nbytes / 1e6:.0f} MB) stay in L2 between steps, so this is "
+                  "not an HBM fraction"}
 
 
 def multi_token_decode(args, gdn, flush, stream, dev, N=128, T=4):

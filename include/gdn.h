@@ -179,7 +179,9 @@ GDN_API int gdn_decode_step_slots(const void *q, const void *k, const void *v, c
  * `stream`, and work queued on `stream` afterwards starts after the last copy (so
  * synchronising `stream` means the host outputs are written). Calls from several host
  * threads on one device are serialised while they queue work.
- * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA. Argument and
+ * size errors are returned before anything is queued; a GDN_ERR_CUDA from a CUDA call
+ * made while queueing may leave the copies and launches queued before it in flight.
  */
 GDN_API int gdn_prefill_from_host(const void *q_h, const void *k_h, const void *v_h, const void *g_h,
                           const void *b_h, const float *state_in_h, float *state_out_h, void *out_h,

@@ -3,6 +3,8 @@
 // queued; a failed check returns its gdn_status and touches nothing.
 #include <stdint.h>
 
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "gdn.h"
@@ -18,9 +20,12 @@ __device__ int g_device_status = 0;
 constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices] = {nullptr};
 
+std::mutex g_status_mu;  // first use on a device may come from several host threads
+
 int *status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
     if (!g_status_ptr[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;

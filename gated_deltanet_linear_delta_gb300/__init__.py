@@ -9,6 +9,12 @@ built, every call raises.
 Tensors are torch CUDA tensors, contiguous, in the layouts of ``gdn.h``:
 q, k [Ttot, Hk, dk]; v, out [Ttot, Hv, dv]; g, b [Ttot, Hv] (bf16 or fp32,
 all the same dtype); states [B, Hv, dv, dk] fp32; cu_seqlens int32 [B+1].
+
+The per-call host cost is kept small because a decode step of a few
+sequences runs in a few microseconds on the GPU: the library handle and its
+function objects are looked up once, pointers go to ctypes as plain integers,
+and the current stream is read as a raw handle. Size and alignment checks are
+the C library's (it returns an error before queueing anything).
 """
 from __future__ import annotations
 
@@ -20,7 +26,8 @@ import torch
 
 from . import _build
 
-__all__ = ["GDNError", "gdn_prefill", "gdn_prefill_from_host", "gdn_decode_step", "gdn_decode_step_slots", "gdn_prepass", "gdn_prefill_path",
+__all__ = ["GDNError", "gdn_prefill", "gdn_prefill_ws", "gdn_prefill_workspace_size", "gdn_prefill_from_host",
+           "gdn_decode_step", "gdn_decode_step_slots", "gdn_prepass", "gdn_prefill_path",
            "gdn_get_device_status", "gdn_status_string", "library", "library_path",
            "GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
            "GDN_ERR_DEVICE_CHECK", "GDN_BF16", "GDN_F32"]
@@ -33,6 +40,9 @@ _lib: ctypes.CDLL | None = None
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+_DTYPE = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
+# the current stream of a device as a raw cudaStream_t (falls back to the Stream object)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 class GDNError(RuntimeError):
@@ -48,6 +58,9 @@ def library_path() -> str:
 def library() -> ctypes.CDLL:
     """Load libgdn_gb300.so (built by ``__graft_entry__.build()``); raise if it is missing."""
     global _lib
+    lib = _lib
+    if lib is not None:
+        return lib
     with _lock:
         if _lib is None:
             path = library_path()
@@ -56,6 +69,10 @@ def library() -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             lib.gdn_prefill.argtypes = [_P] * 9 + [_I] * 8 + [_P]
             lib.gdn_prefill.restype = _I
+            lib.gdn_prefill_ws.argtypes = [_P] * 9 + [_I] * 8 + [_P, ctypes.c_size_t, _P]
+            lib.gdn_prefill_ws.restype = _I
+            lib.gdn_prefill_workspace_size.argtypes = [_I] * 8
+            lib.gdn_prefill_workspace_size.restype = ctypes.c_size_t
             lib.gdn_decode_step.argtypes = [_P] * 7 + [_I] * 6 + [_P]
             lib.gdn_decode_step.restype = _I
             lib.gdn_prefill_from_host.argtypes = [_P] * 15 + [_I] * 8 + [_P]
@@ -79,25 +96,27 @@ def gdn_status_string(status: int) -> str:
 
 
 def _dtype_code(t: torch.Tensor) -> int:
-    if t.dtype == torch.bfloat16:
-        return GDN_BF16
-    if t.dtype == torch.float32:
-        return GDN_F32
-    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+    code = _DTYPE.get(t.dtype)
+    if code is None:
+        raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+    return code
 
 
 def _ptr(t: torch.Tensor | None):
     if t is None:
         return None
-    if not t.is_cuda or not t.is_contiguous():
+    if not (t.is_cuda and t.is_contiguous()):
         raise ValueError("tensors must be contiguous CUDA tensors")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream, t: torch.Tensor | None = None):
+    """cudaStream_t of `stream`, or of the current stream of t's device (None: the current device)."""
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(t.get_device() if t is not None else torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _check(rc: int, where: str) -> None:
@@ -105,9 +124,7 @@ def _check(rc: int, where: str) -> None:
         raise GDNError(rc, where)
 
 
-def gdn_prefill(q, k, v, g, b, state_in, state_out, out, cu_seqlens=None, B=None, T=None, chunk=64,
-                stream=None) -> None:
-    """Chunked prefill over packed sequences; writes `out` and `state_out` (may alias state_in)."""
+def _prefill_sizes(q, v, g, b, out, state_in, state_out, cu_seqlens, B, T):
     Ttot, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     if cu_seqlens is not None:
@@ -117,17 +134,46 @@ def gdn_prefill(q, k, v, g, b, state_in, state_out, out, cu_seqlens=None, B=None
     else:
         B = 1 if B is None else B
         T = Ttot // B if T is None else T
-    dt = _dtype_code(q)
-    for t in (k, v, g, b, out):
+    for t in (v, g, b, out):
         if t.dtype != q.dtype:
             raise TypeError("q, k, v, g, b and out must share one dtype")
     for t in (state_in, state_out):
         if t is not None and t.dtype != torch.float32:
             raise TypeError("states are fp32")
-    rc = library().gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_in),
-                               _ptr(state_out), _ptr(out), _ptr(cu_seqlens), B, T, Hk, Hv, dk, dv,
-                               chunk, dt, _stream(stream))
+    return B, T, Hk, Hv, dk, dv
+
+
+def gdn_prefill(q, k, v, g, b, state_in, state_out, out, cu_seqlens=None, B=None, T=None, chunk=64,
+                stream=None) -> None:
+    """Chunked prefill over packed sequences; writes `out` and `state_out` (may alias state_in)."""
+    lib = _lib or library()
+    if k.dtype != q.dtype:
+        raise TypeError("q, k, v, g, b and out must share one dtype")
+    B, T, Hk, Hv, dk, dv = _prefill_sizes(q, v, g, b, out, state_in, state_out, cu_seqlens, B, T)
+    rc = lib.gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_in), _ptr(state_out), _ptr(out),
+                         _ptr(cu_seqlens), B, T, Hk, Hv, dk, dv, chunk, _dtype_code(q), _stream(stream, q))
     _check(rc, "gdn_prefill")
+
+
+def gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype) -> int:
+    """Bytes of device workspace gdn_prefill_ws needs for these sizes (0: none)."""
+    if isinstance(dtype, torch.dtype):
+        dtype = _DTYPE[dtype]
+    return int(library().gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, int(dtype)))
+
+
+def gdn_prefill_ws(q, k, v, g, b, state_in, state_out, out, workspace, cu_seqlens=None, B=None, T=None, chunk=64,
+                   stream=None) -> None:
+    """gdn_prefill with a caller-owned device workspace (a uint8 CUDA tensor, or None when none is needed)."""
+    lib = _lib or library()
+    if k.dtype != q.dtype:
+        raise TypeError("q, k, v, g, b and out must share one dtype")
+    B, T, Hk, Hv, dk, dv = _prefill_sizes(q, v, g, b, out, state_in, state_out, cu_seqlens, B, T)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.gdn_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_in), _ptr(state_out), _ptr(out),
+                            _ptr(cu_seqlens), B, T, Hk, Hv, dk, dv, chunk, _dtype_code(q), _ptr(workspace), nbytes,
+                            _stream(stream, q))
+    _check(rc, "gdn_prefill_ws")
 
 
 def _host_ptr(t: torch.Tensor | None):
@@ -135,7 +181,7 @@ def _host_ptr(t: torch.Tensor | None):
         return None
     if t.is_cuda or not t.is_contiguous():
         raise ValueError("host arrays must be contiguous CPU tensors")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def gdn_prefill_from_host(q, k, v, g, b, state_in, state_out, out, dev, chunk=64, fragment=1024,
@@ -152,34 +198,37 @@ def gdn_prefill_from_host(q, k, v, g, b, state_in, state_out, out, dev, chunk=64
         _host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(g), _host_ptr(b), _host_ptr(state_in),
         _host_ptr(state_out), _host_ptr(out), _ptr(dev["q"]), _ptr(dev["k"]), _ptr(dev["v"]), _ptr(dev["g"]),
         _ptr(dev["b"]), _ptr(dev["state"]), _ptr(dev["out"]), T, Hk, Hv, dk, dv, chunk, _dtype_code(q),
-        fragment, _stream(stream))
+        fragment, _stream(stream, dev["q"]))
     _check(rc, "gdn_prefill_from_host")
 
 
 def gdn_decode_step(q, k, v, g, b, state, out, stream=None) -> None:
     """One decode step for N sequences; updates `state` in place and writes `out`."""
+    lib = _lib or library()
     N, Hk, dk = q.shape
-    Hv, dv = v.shape[1], v.shape[2]
-    dt = _dtype_code(q)
+    _, Hv, dv = v.shape
     if state.dtype != torch.float32:
         raise TypeError("the state is fp32")
-    rc = library().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state), _ptr(out),
-                                   N, Hk, Hv, dk, dv, dt, _stream(stream))
-    _check(rc, "gdn_decode_step")
+    rc = lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state), _ptr(out),
+                             N, Hk, Hv, dk, dv, _dtype_code(q), _stream(stream, q))
+    if rc:
+        raise GDNError(rc, "gdn_decode_step")
 
 
 def gdn_decode_step_slots(q, k, v, g, b, state_pool, slots, out, stream=None) -> None:
     """One decode step; sequence n updates state_pool[slots[n]] in place (slots[n] < 0: padding)."""
+    lib = _lib or library()
     N, Hk, dk = q.shape
-    Hv, dv = v.shape[1], v.shape[2]
+    _, Hv, dv = v.shape
     if state_pool.dtype != torch.float32:
         raise TypeError("the state pool is fp32")
     if slots.dtype != torch.int32 or slots.numel() != N:
         raise TypeError("slots must be int32 with one entry per sequence")
-    rc = library().gdn_decode_step_slots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_pool),
-                                         _ptr(slots), _ptr(out), N, state_pool.shape[0], Hk, Hv, dk, dv,
-                                         _dtype_code(q), _stream(stream))
-    _check(rc, "gdn_decode_step_slots")
+    rc = lib.gdn_decode_step_slots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_pool), _ptr(slots),
+                                   _ptr(out), N, state_pool.shape[0], Hk, Hv, dk, dv, _dtype_code(q),
+                                   _stream(stream, q))
+    if rc:
+        raise GDNError(rc, "gdn_decode_step_slots")
 
 
 def gdn_prepass(q, k, g, b, rq, rk, beta, gcum, cu_seqlens=None, B=None, T=None, chunk=64,
@@ -194,7 +243,7 @@ def gdn_prepass(q, k, g, b, rq, rk, beta, gcum, cu_seqlens=None, B=None, T=None,
         T = Ttot // B if T is None else T
     rc = library().gdn_prepass(_ptr(q), _ptr(k), _ptr(g), _ptr(b), _ptr(cu_seqlens), B, T, Hk, Hv, dk,
                                chunk, _dtype_code(q), _ptr(rq), _ptr(rk), _ptr(beta), _ptr(gcum),
-                               _stream(stream))
+                               _stream(stream, q))
     _check(rc, "gdn_prepass")
 
 

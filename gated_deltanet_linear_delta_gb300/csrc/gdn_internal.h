@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace gdn {
@@ -42,6 +43,11 @@ cudaError_t launch_prepass(const PrepassArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);
+// tensor-core kernel with the one-product state chain and block preparation spread over the GPU;
+// needs a device workspace of prefill_ring_workspace(a) bytes (1 KiB aligned)
+bool prefill_ring_supported(const PrefillArgs &a);
+size_t prefill_ring_workspace(const PrefillArgs &a);
+cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
 bool prefill_scan_supported(const PrefillArgs &a);
 cudaError_t launch_prefill_scan(const PrefillArgs &a, cudaStream_t s);
 

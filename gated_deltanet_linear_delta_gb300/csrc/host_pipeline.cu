@@ -28,6 +28,7 @@ struct DevicePipe {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
     cudaEvent_t start = nullptr, done_in[kMaxFragments] = {}, done_k[kMaxFragments] = {}, done_out = nullptr;
+    cudaEvent_t join_in = nullptr, join_out = nullptr;  // error path: the caller's stream waits for both
 };
 DevicePipe g_pipe[kMaxDevices];
 std::mutex g_init_mu;
@@ -44,6 +45,8 @@ DevicePipe *pipe_for_device() {
     const unsigned fl = cudaEventDisableTiming;
     if (cudaEventCreateWithFlags(&d.start, fl) != cudaSuccess) return nullptr;
     if (cudaEventCreateWithFlags(&d.done_out, fl) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&d.join_in, fl) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&d.join_out, fl) != cudaSuccess) return nullptr;
     for (int f = 0; f < kMaxFragments; ++f)
         if (cudaEventCreateWithFlags(&d.done_in[f], fl) != cudaSuccess ||
             cudaEventCreateWithFlags(&d.done_k[f], fl) != cudaSuccess)
@@ -86,10 +89,20 @@ extern "C" int gdn_prefill_from_host(const void *q_h, const void *k_h, const voi
     if (!ok(cudaEventRecord(d->start, sk)) || !ok(cudaStreamWaitEvent(d->in, d->start, 0)) ||
         !ok(cudaStreamWaitEvent(d->out, d->start, 0)))
         return GDN_ERR_CUDA;
+    // After the first copy is queued, a failing step still joins both library streams into the
+    // caller's stream before returning, so that work the caller queues next (or a synchronisation
+    // of its stream) also waits for the copies already in flight into or out of its buffers.
+    auto fail = [&](int code) {
+        cudaEventRecord(d->join_in, d->in);
+        cudaEventRecord(d->join_out, d->out);
+        cudaStreamWaitEvent(sk, d->join_in, 0);
+        cudaStreamWaitEvent(sk, d->join_out, 0);
+        return code;
+    };
     if (state_in_h) {
-        if (!ok(cudaMemcpyAsync(state_d, state_in_h, st_bytes, cudaMemcpyHostToDevice, d->in))) return GDN_ERR_CUDA;
+        if (!ok(cudaMemcpyAsync(state_d, state_in_h, st_bytes, cudaMemcpyHostToDevice, d->in))) return fail(GDN_ERR_CUDA);
     } else if (nfrag == 0) {  // an empty prompt passes a zero state through
-        if (!ok(cudaMemsetAsync(state_d, 0, st_bytes, d->in))) return GDN_ERR_CUDA;
+        if (!ok(cudaMemsetAsync(state_d, 0, st_bytes, d->in))) return fail(GDN_ERR_CUDA);
     }
     for (int f = 0; f < nfrag; ++f) {
         const size_t t0 = (size_t)f * fragment;
@@ -99,23 +112,23 @@ extern "C" int gdn_prefill_from_host(const void *q_h, const void *k_h, const voi
         for (const auto &x : in)
             if (!ok(cudaMemcpyAsync(m8(x.dv, t0 * x.tok), c8(x.h, t0 * x.tok), n * x.tok, cudaMemcpyHostToDevice,
                                     d->in)))
-                return GDN_ERR_CUDA;
+                return fail(GDN_ERR_CUDA);
         if (!ok(cudaEventRecord(d->done_in[f], d->in)) || !ok(cudaStreamWaitEvent(sk, d->done_in[f], 0)))
-            return GDN_ERR_CUDA;
+            return fail(GDN_ERR_CUDA);
         const bool first = f == 0;
         rc = gdn_prefill(m8(q_d, t0 * qk_tok), m8(k_d, t0 * qk_tok), m8(v_d, t0 * v_tok), m8(g_d, t0 * g_tok),
                          m8(b_d, t0 * g_tok), first && !state_in_h ? nullptr : state_d, state_d,
                          m8(out_d, t0 * v_tok), nullptr, 1, (int)n, Hk, Hv, dk, dv, chunk, dtype, sk);
-        if (rc != GDN_OK) return rc;
+        if (rc != GDN_OK) return fail(rc);
         if (!ok(cudaEventRecord(d->done_k[f], sk)) || !ok(cudaStreamWaitEvent(d->out, d->done_k[f], 0)) ||
             !ok(cudaMemcpyAsync(m8(out_h, t0 * v_tok), c8(out_d, t0 * v_tok), n * v_tok, cudaMemcpyDeviceToHost,
                                 d->out)))
-            return GDN_ERR_CUDA;
+            return fail(GDN_ERR_CUDA);
     }
     if (nfrag == 0 && (!ok(cudaEventRecord(d->done_in[0], d->in)) || !ok(cudaStreamWaitEvent(d->out, d->done_in[0], 0))))
-        return GDN_ERR_CUDA;
+        return fail(GDN_ERR_CUDA);
     if (!ok(cudaMemcpyAsync(state_out_h, state_d, st_bytes, cudaMemcpyDeviceToHost, d->out)) ||
         !ok(cudaEventRecord(d->done_out, d->out)) || !ok(cudaStreamWaitEvent(sk, d->done_out, 0)))
-        return GDN_ERR_CUDA;
+        return fail(GDN_ERR_CUDA);
     return GDN_OK;
 }

@@ -37,7 +37,7 @@ template <int DK, int DVS, int C, typename TIn>
 __global__ void __launch_bounds__(kSimtThreads)
 prefill_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
                     const TIn *__restrict__ g, const TIn *__restrict__ b,
-                    const float *__restrict__ state_in, float *__restrict__ state_out,
+                    const float *state_in, float *state_out,  // may alias (in-place update)
                     TIn *__restrict__ out, const int32_t *__restrict__ cu, int B, long T, long Ttot,
                     int Hk, int Hv, int DV, int *status) {
     using L = SimtSmem<DK, DVS, C>;

@@ -119,11 +119,6 @@ constexpr uint32_t TM_AU = 448;   // chain: fp16 U^T               (32)
 constexpr uint32_t CT_X1 = 0, CT_X2O = 64, CT_Q = 128, CT_S = 192, CT_AS = 320, CT_AUH = 384, CT_AUL = 416,
                    CT_AUF = 448;
 
-// instruction descriptor, kind::f16 with fp16 operands and an fp32 accumulator
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
-    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
 constexpr uint32_t ID_GRAM_BF16 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_W = idesc_f16(128, 64, 1, 0);
 constexpr uint32_t ID_X1 = idesc_f16(128, 64, 1, 0);
@@ -147,83 +142,6 @@ struct TcParams {
     int F;  // first rank that prepares blocks: block k is prepared by rank F + k % (P - F)
 };
 
-// ---- small helpers ----
-__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-// barrier that also returns, to every participant, whether any of them passed `pred` true:
-// a give-up decision that all threads of a group take together
-__device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    mma_bf16(d, a, b, idesc, acc);  // same instruction; the operand type is in the idesc
-}
-__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// bf16 operands, A from TMEM: the same instruction, the operand type is in the idesc
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-    mma_f16_ts(d, a_tmem, b, idesc, acc);
-}
-// 32 lanes x 16 consecutive columns
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
-}
-__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t h2_bits(float a, float b) {
-    __half2 v = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-__device__ __forceinline__ uint4 pack8_f16(const float *x, float s) {
-    return make_uint4(h2_bits(s * x[0], s * x[1]), h2_bits(s * x[2], s * x[3]), h2_bits(s * x[4], s * x[5]),
-                      h2_bits(s * x[6], s * x[7]));
-}
-// exact power of two 2^(14 - e) with m < 2^e: m * scale < 2^14 (fp16 max 65504)
-__device__ __forceinline__ float pow2_scale(float m) {
-    if (!(m > 0.f) || !isfinite(m)) return 1.f;
-    int e;
-    frexpf(m, &e);
-    e = max(-100, min(100, 14 - e));
-    return ldexpf(1.f, e);
-}
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
-}
 // fp32 64 x 64 row-major with the column index XOR-swizzled by the row (keeps float4 groups)
 __device__ __forceinline__ int sw(int t, int s) { return t * 64 + (s ^ ((t & 7) << 2)); }
 

@@ -40,6 +40,7 @@
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -97,11 +98,48 @@ typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
  * token scan instead: every state row is read once, takes the T updates in
  * order in registers, and is written once, so T steps cost one pass over the
  * state. The result is the same function (only the rounding order differs).
- * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
+ * The tensor-core path needs device scratch (see gdn_prefill_workspace_size); gdn_prefill
+ * keeps one workspace per device for it, allocated by the first call that needs it and grown
+ * (after the work using the old one has finished) when a call needs more. Calls on different
+ * streams are ordered on the GPU so that they never use it at once. Inside a stream capture
+ * no allocation and no cross-stream ordering can be made: make one call of the same sizes (or
+ * larger) outside the capture first, and do not let a captured prefill run at the same time as
+ * another prefill of the same device; otherwise use gdn_prefill_ws with a workspace per stream.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA (also when the
+ * workspace cannot be allocated, or would have to be inside a stream capture).
  */
 GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void *g, const void *b,
                 const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
                 int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype, void *stream);
+
+/*
+ * gdn_prefill_workspace_size -- bytes of device workspace gdn_prefill_ws needs for these
+ * sizes, with or without cu_seqlens (0: the kernel for these sizes needs none, or the sizes are
+ * invalid).
+ *
+ * The tensor-core prefill (dk = dv = 128, chunk 64, bf16) splits the GPU into CTAs that carry
+ * the states and CTAs that prepare blocks for them, which hand each block's operands over
+ * through a ring of slots in device memory; the workspace holds that ring (a fixed 96 KiB per
+ * slot, 3 slots per state-carrying CTA) plus per-call tables that grow with B and Hv. It is
+ * scratch: nothing in it outlives a call. Host-only, no device work.
+ */
+GDN_API size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, int chunk,
+                                          int dtype);
+
+/*
+ * gdn_prefill_ws -- gdn_prefill with a caller-owned workspace.
+ *
+ * Same arguments and result as gdn_prefill, plus `workspace`: DEVICE memory of at least
+ * gdn_prefill_workspace_size(...) bytes, 256-byte aligned (as cudaMalloc returns), which the
+ * call uses as scratch until its work on `stream` has finished. Calls whose work may overlap
+ * on the GPU must use different workspaces. When the size function returns 0, `workspace`
+ * may be NULL. Returns GDN_ERR_INVALID_ARG when the workspace is missing, too small or
+ * misaligned; otherwise as gdn_prefill.
+ */
+GDN_API int gdn_prefill_ws(const void *q, const void *k, const void *v, const void *g, const void *b,
+                           const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
+                           int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * gdn_decode_step -- one recurrent step for N independent sequences.
@@ -180,8 +218,10 @@ GDN_API int gdn_decode_step_slots(const void *q, const void *k, const void *v, c
  * synchronising `stream` means the host outputs are written). Calls from several host
  * threads on one device are serialised while they queue work.
  * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA. Argument and
- * size errors are returned before anything is queued; a GDN_ERR_CUDA from a CUDA call
- * made while queueing may leave the copies and launches queued before it in flight.
+ * size errors are returned before anything is queued. An error from a CUDA call made while
+ * queueing may leave the copies and launches queued before it in flight; the call still makes
+ * `stream` wait for them before it returns, so the caller's buffers are free once `stream`'s
+ * later work runs (or `stream` is synchronised).
  */
 GDN_API int gdn_prefill_from_host(const void *q_h, const void *k_h, const void *v_h, const void *g_h,
                           const void *b_h, const float *state_in_h, float *state_out_h, void *out_h,
@@ -218,6 +258,11 @@ GDN_API int gdn_prefill_path(int B, int T, int Hk, int Hv, int dk, int dv, int c
  * device status word: GDN_OK, or GDN_ERR_DEVICE_CHECK if a kernel found
  * inconsistent device data since the last call; GDN_ERR_CUDA if the
  * synchronisation itself failed.
+ * There is one status word per device, shared by every stream and every call
+ * on that device: a flag raised by work on another stream is reported to
+ * whichever caller reads the word first. The word is read and cleared in one
+ * atomic step (a one-thread kernel on `stream`), so no flag is lost between
+ * the read and the clear.
  */
 GDN_API int gdn_get_device_status(void *stream);
 

@@ -78,6 +78,7 @@ def test_varlen_edges_qwen_heads(lengths):
 def test_cluster_splits(split, monkeypatch):
     """With few heads, a cluster of P CTAs per value head prepares the blocks (ranks F..P-1 in
     turn) for the CTA that carries the state: every split gives the oracle's result."""
+    monkeypatch.setenv("GDN_PREFILL_KERNEL", "cluster")
     monkeypatch.setenv("GDN_PREFILL_CLUSTER", split)
     b = inputs.make_batch(Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", chunk=64, seed=21, init_state=True,
                           slow_gate=True, lengths=[0, 1, 63, 64, 65, 130, 7, 700])

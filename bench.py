@@ -46,7 +46,9 @@ PREFILL_FLOPS_PER_TOKEN = HV * (5 * 2 * CHUNK * DK + 3 * 2 * DK * DV)  # chunk G
 DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + IO_BYTES_PER_TOKEN
 # DRAM bytes per launch from the committed ncu captures (profiles/); None once a kernel
 # has changed since its capture.
-TRAFFIC = {"prefill": 77.29e6, "decode": 480.2e6, "scan": 488.3e6}
+TRAFFIC = {"prefill": None, "decode": 480.2e6, "scan": 488.3e6}
+# nominal GB300 figures, reported beside the measured denominators
+NOMINAL_HBM_GBS, NOMINAL_BF16_TFLOPS = 7900.0, 2250.0
 
 
 def peaks():
@@ -220,9 +222,13 @@ def run_ours(args, rank, world):
     achieved_gbs = PREFILL_BYTES / pre_s / 1e9
     achieved_tfs = PREFILL_FLOPS_PER_TOKEN * T_PREFILL / pre_s / 1e12
     roof_time = max(PREFILL_BYTES / (hbm * 1e9), PREFILL_FLOPS_PER_TOKEN * T_PREFILL / (bf16 * 1e12))
+    roof_nom = max(PREFILL_BYTES / (NOMINAL_HBM_GBS * 1e9),
+                   PREFILL_FLOPS_PER_TOKEN * T_PREFILL / (NOMINAL_BF16_TFLOPS * 1e12))
     dec_bytes = N_DECODE * DECODE_BYTES_PER_SEQ
     dec_gbs = dec_bytes / (dec_mean / 1e3) / 1e9
     path = gdn.gdn_prefill_path(1, T_PREFILL, HK, HV, DK, DV, CHUNK, gdn.GDN_BF16)
+    # the tensor-core path launches a planning kernel then the block kernel
+    prefill_launches = 2 if path == 1 else 1
     clocks = clk.summary()
     value = job_throughput(world, T_PREFILL, pre_s) / 1e6
     line = {
@@ -233,24 +239,26 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "prefill_tokens": T_PREFILL, "decode_batch": N_DECODE,
                    "Hk": HK, "Hv": HV, "dk": DK, "dv": DV, "chunk": CHUNK,
                    "l2": "flushed: 256 MiB write before each timed launch",
-                   "prefill_kernel": {1: "tcgen05 block kernel", 0: "CUDA-core block kernel"}.get(path, path),
+                   "prefill_kernel": {1: "tcgen05 ring kernel (block preparation + state chains)",
+                                      0: "CUDA-core block kernel"}.get(path, path),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "prefill": {"ms": round(pre_mean, 5), "Mtok_s": round(T_PREFILL / pre_s / 1e6, 3),
                     "GB_s": round(achieved_gbs, 1), "TFLOP_s": round(achieved_tfs, 2),
-                    "roofline_ms": round(roof_time * 1e3, 5), "frac_of_roofline": round(roof_time / pre_s, 4)},
+                    "roofline_ms": round(roof_time * 1e3, 5), "frac_of_roofline": round(roof_time / pre_s, 4),
+                    "frac_of_nominal_roofline": round(roof_nom / pre_s, 4)},
         "decode": {"value": round(dec_mean * 1e3, 3), "unit": "us/step", "batch": N_DECODE,
                    "higher_is_better": False, "GB_s": round(dec_gbs, 1),
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                                 "frac": round(dec_gbs / hbm, 4), "traffic": TRAFFIC["decode"],
-                                "peak_source": src},
+                                "peak_source": src, "frac_of_nominal": round(dec_gbs / NOMINAL_HBM_GBS, 4)},
                    "sweep_us": sweep, "graph": graph, "multi_token": multi, "copy_reference": copy_ref},
         "other_workloads": other,
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved_gbs / hbm, 4), "traffic": TRAFFIC["prefill"], "peak_source": src,
-                     "kernel": "prefill"},
+                     "kernel": "prefill", "frac_of_nominal": round(achieved_gbs / NOMINAL_HBM_GBS, 4)},
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (prefill_launches + 1) * args.steps,
         "wall_s_timed_region": round(wall, 4),
     }
     return line
@@ -279,15 +287,14 @@ def copy_reference(args, flush, stream, dev):
 
 
 def other_prefill_workloads(args, gdn, flush, stream, dev, reps=5):
-    """The other prefill workloads (reported, not the headline): one 32768-token sequence with a
-    seeded initial state, and 16 packed sequences of lengths U{256..16384} with their own states
-    (131072 tokens with --all-workloads). L2 flushed before each launch; median of `reps`."""
+    """The other prefill workloads (reported, not the headline): one 32768-token and one
+    131072-token sequence with a seeded initial state, and 16 packed sequences of lengths
+    U{256..16384} with their own states. L2 flushed before each launch; median of `reps`."""
     from gated_deltanet_linear_delta_gb300 import inputs
     hbm, bf16, src = peaks()
     cases = [("T=32768, seeded state", lambda: inputs.prefill_long(T=32768)),
+             ("T=131072, seeded state", lambda: inputs.prefill_long(T=131072)),
              ("varlen 16 seqs U{256..16384}, seeded states", inputs.prefill_varlen)]
-    if args.all_workloads:
-        cases.append(("T=131072, seeded state", lambda: inputs.prefill_long(T=131072)))
     res = {}
     for name, make in cases:
         b = make().to(dev)
@@ -308,9 +315,11 @@ def other_prefill_workloads(args, gdn, flush, stream, dev, reps=5):
         ms = sorted(a.elapsed_time(c) for a, c in ev)[len(ev) // 2]
         nbytes = ntok * IO_BYTES_PER_TOKEN + 2 * b.B * STATE_BYTES
         roof = max(nbytes / (hbm * 1e9), ntok * PREFILL_FLOPS_PER_TOKEN / (bf16 * 1e12))
+        roof_nom = max(nbytes / (NOMINAL_HBM_GBS * 1e9), ntok * PREFILL_FLOPS_PER_TOKEN / (NOMINAL_BF16_TFLOPS * 1e12))
         res[name] = {"tokens": ntok, "ms": round(ms, 4), "Mtok_s": round(ntok / ms / 1e3, 3),
                      "GB_s": round(nbytes / ms / 1e6, 1), "roofline_ms": round(roof * 1e3, 4),
-                     "frac_of_roofline": round(roof * 1e3 / ms, 4)}
+                     "frac_of_roofline": round(roof * 1e3 / ms, 4),
+                     "frac_of_nominal_roofline": round(roof_nom * 1e3 / ms, 4)}
         if b.cu_seqlens is not None:  # then 128 decode steps on the sequences' final states
             res[name]["then_128_decode_steps"] = decode_after_prefill(gdn, so, stream, dev, steps=128)
         del b, out, so
@@ -386,12 +395,14 @@ def multi_token_decode(args, gdn, flush, stream, dev, N=128, T=4):
 def decode_graph_sweep(gdn, qkvgb, dstate, dout, stream, G=32, reps=20):
     """Decode steps back to back (the state updated in place, L2 warm): G launches issued eagerly
     against the same G launches captured once in a CUDA graph and replayed; us per step."""
-    qd, kd, vd, gd, bd = qkvgb
     res = {"steps_per_graph": G, "l2": "warm (consecutive steps, no flush)"}
     for n in (1, 8, 32, 128):
+        # views taken once, outside the timed loops: eager_us is the binding's call plus the launch
+        qn, kn, vn, gn, bn, sn, on = (x[:n] for x in (*qkvgb, dstate, dout))
+
         def steps():
             for _ in range(G):
-                gdn.gdn_decode_step(qd[:n], kd[:n], vd[:n], gd[:n], bd[:n], dstate[:n], dout[:n])
+                gdn.gdn_decode_step(qn, kn, vn, gn, bn, sn, on)
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -417,7 +428,36 @@ def decode_graph_sweep(gdn, qkvgb, dstate, dout, stream, G=32, reps=20):
         res[str(n)] = {"eager_us": round(1e3 * ev[0].elapsed_time(ev[1]) / (reps * G), 3),
                        "graph_us": round(1e3 * ev[2].elapsed_time(ev[3]) / (reps * G), 3)}
         del graph
+    res["host_us"] = host_call_cost(gdn, qkvgb, dstate, dout)
     return res
+
+
+def host_call_cost(gdn, qkvgb, dstate, dout, calls=2000):
+    """Host time per call (no GPU wait): a bare ctypes call into the library that does no CUDA
+    work (gdn_prefill_path), the library's gdn_decode_step reached through ctypes with
+    prepared integer arguments, and the Python binding's gdn_decode_step (argument
+    marshalling included), for one sequence."""
+    lib = gdn.library()
+    n = 1
+    qn, kn, vn, gn, bn, sn, on = (x[:n] for x in (*qkvgb, dstate, dout))
+    hk, dk = qn.shape[1], qn.shape[2]
+    hv, dv = vn.shape[1], vn.shape[2]
+    raw = torch.cuda.current_stream().cuda_stream
+    ptrs = [t.data_ptr() for t in (qn, kn, vn, gn, bn, sn, on)]
+
+    def per_call(fn):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        dt = time.perf_counter() - t0
+        torch.cuda.synchronize()
+        return round(1e6 * dt / calls, 3)
+    return {"bare_ctypes_us": per_call(lambda: lib.gdn_prefill_path(1, 64, hk, hv, dk, dv, 64, gdn.GDN_BF16)),
+            "ctypes_decode_us": per_call(lambda: lib.gdn_decode_step(*ptrs, n, hk, hv, dk, dv, gdn.GDN_BF16, raw)),
+            "binding_decode_us": per_call(lambda: gdn.gdn_decode_step(qn, kn, vn, gn, bn, sn, on)),
+            "calls": calls}
 
 
 E2E_FRAGMENT = 1024  # tokens per fragment of the host-to-host prefill
@@ -502,7 +542,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--all-workloads", action="store_true", help="also time the 131072-token prompt")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

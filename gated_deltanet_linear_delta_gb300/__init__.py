@@ -26,7 +26,8 @@ import torch
 
 from . import _build
 
-__all__ = ["GDNError", "gdn_prefill", "gdn_prefill_ws", "gdn_prefill_workspace_size", "gdn_prefill_from_host",
+__all__ = ["GDNError", "gdn_prefill", "gdn_prefill_ws", "gdn_prefill_workspace_size", "gdn_prefill_static",
+           "gdn_prefill_from_host",
            "gdn_decode_step", "gdn_decode_step_slots", "gdn_prepass", "gdn_prefill_path",
            "gdn_get_device_status", "gdn_status_string", "library", "library_path",
            "GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
@@ -69,6 +70,8 @@ def library() -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             lib.gdn_prefill.argtypes = [_P] * 9 + [_I] * 8 + [_P]
             lib.gdn_prefill.restype = _I
+            lib.gdn_prefill_static.argtypes = [_P] * 9 + [_I] * 8 + [_P]
+            lib.gdn_prefill_static.restype = _I
             lib.gdn_prefill_ws.argtypes = [_P] * 9 + [_I] * 8 + [_P, ctypes.c_size_t, _P]
             lib.gdn_prefill_ws.restype = _I
             lib.gdn_prefill_workspace_size.argtypes = [_I] * 8
@@ -153,6 +156,20 @@ def gdn_prefill(q, k, v, g, b, state_in, state_out, out, cu_seqlens=None, B=None
     rc = lib.gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_in), _ptr(state_out), _ptr(out),
                          _ptr(cu_seqlens), B, T, Hk, Hv, dk, dv, chunk, _dtype_code(q), _stream(stream, q))
     _check(rc, "gdn_prefill")
+
+
+def gdn_prefill_static(q, k, v, g, b, state_in, state_out, out, cu_seqlens=None, B=None, T=None, chunk=64,
+                       stream=None) -> None:
+    """gdn_prefill that allocates nothing at call time: the tensor-core path's scratch is a fixed
+    array in the library's device image, shared by all calls on a device (overlapping calls race)."""
+    lib = _lib or library()
+    if k.dtype != q.dtype:
+        raise TypeError("q, k, v, g, b and out must share one dtype")
+    B, T, Hk, Hv, dk, dv = _prefill_sizes(q, v, g, b, out, state_in, state_out, cu_seqlens, B, T)
+    rc = lib.gdn_prefill_static(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(state_in), _ptr(state_out),
+                                _ptr(out), _ptr(cu_seqlens), B, T, Hk, Hv, dk, dv, chunk, _dtype_code(q),
+                                _stream(stream, q))
+    _check(rc, "gdn_prefill_static")
 
 
 def gdn_prefill_workspace_size(B, T, Hk, Hv, dk, dv, chunk, dtype) -> int:

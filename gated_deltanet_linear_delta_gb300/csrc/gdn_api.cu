@@ -176,6 +176,29 @@ int gdn_prefill_ws(const void *q, const void *k, const void *v, const void *g, c
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+int gdn_prefill_static(const void *q, const void *k, const void *v, const void *g, const void *b,
+                       const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
+                       int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype, void *stream) {
+    int rc = prefill_checks(q, k, v, g, b, state_in, state_out, out, cu_seqlens, B, T, Hk, Hv, dk,
+                            dv, chunk, dtype);
+    if (rc != GDN_OK) return rc;
+    if (B == 0) return GDN_OK;
+    gdn::PrefillArgs a{q, k, v, g, b, state_in, state_out, out, cu_seqlens, B, T, Hk, Hv, dk, dv, chunk, dtype,
+                       nullptr};
+    // sizes whose kernels take no scratch: the same kernels as gdn_prefill, nothing allocated
+    if (gdn::prefill_scan_supported(a) || !gdn::prefill_ring_supported(a))
+        return gdn_prefill_ws(q, k, v, g, b, state_in, state_out, out, cu_seqlens, B, T, Hk, Hv, dk, dv, chunk,
+                              dtype, nullptr, 0, stream);
+    const size_t need = gdn::prefill_ring_workspace(a, gdn::kStaticChainCtas);
+    if (need == 0 || need > gdn::kStaticScratchBytes) return GDN_ERR_UNSUPPORTED;
+    void *scratch = gdn::static_scratch();
+    a.status = status_ptr();
+    if (!scratch || !a.status) return GDN_ERR_CUDA;
+    const cudaError_t e = gdn::launch_prefill_ring(a, scratch, gdn::kStaticScratchBytes,
+                                                   static_cast<cudaStream_t>(stream), gdn::kStaticChainCtas);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int gdn_prefill(const void *q, const void *k, const void *v, const void *g, const void *b,
                 const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
                 int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype, void *stream) {

@@ -44,10 +44,18 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);
 // tensor-core kernel with the one-product state chain and block preparation spread over the GPU;
-// needs a device workspace of prefill_ring_workspace(a) bytes (1 KiB aligned)
+// needs a device workspace of prefill_ring_workspace(a) bytes (256-byte aligned)
 bool prefill_ring_supported(const PrefillArgs &a);
-size_t prefill_ring_workspace(const PrefillArgs &a);
-cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
+// max_chain_ctas > 0 caps the CTAs that carry states (fewer ring slots, a smaller workspace)
+size_t prefill_ring_workspace(const PrefillArgs &a, int max_chain_ctas = 0);
+cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStream_t s,
+                                int max_chain_ctas = 0);
+// Fixed device scratch of the allocation-free prefill: room for the ring of kStaticChainCtas
+// state-carrying CTAs (16 slots of 96 KiB each) plus 1 MiB of per-call tables. static_scratch()
+// returns its address on the current device (looked up on the first call per device), or null.
+constexpr int kStaticChainCtas = 8;
+constexpr size_t kStaticScratchBytes = (size_t)13 << 20;
+void *static_scratch();
 bool prefill_scan_supported(const PrefillArgs &a);
 cudaError_t launch_prefill_scan(const PrefillArgs &a, cudaStream_t s);
 

@@ -74,6 +74,8 @@ constexpr uint32_t RS_BL = 65536;   //   16 KiB B^T lo
 constexpr uint32_t RS_EH = 81920;   //    8 KiB E hi, MN-major [t 0..63][s 0..63]
 constexpr uint32_t RS_EL = 90112;   //    8 KiB E lo
 constexpr uint32_t RS_BYTES = 98304;
+static_assert((size_t)kStaticChainCtas * kSlots * RS_BYTES + ((size_t)1 << 20) <= kStaticScratchBytes,
+              "the fixed scratch holds the ring of its chain CTAs plus 1 MiB of tables");
 
 // ---- chain CTA shared memory (byte offsets from a 1 KiB aligned base) ----
 constexpr uint32_t CH_V = RS_BYTES;                  // raw V tile [i-block 0..1][t][128 B], 16 KiB
@@ -1214,7 +1216,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct RingShape {
     int sms, NC, G, npos;
 };
-bool ring_shape(const PrefillArgs &a, RingShape *sh) {
+bool ring_shape(const PrefillArgs &a, RingShape *sh, int max_chain_ctas) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&sh->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
@@ -1223,6 +1225,7 @@ bool ring_shape(const PrefillArgs &a, RingShape *sh) {
     // about a third of the SMs carry states; the rest prepare blocks. A multiple of r, so that the
     // value heads of one key head sit in consecutive chain CTAs at the same steps.
     long nc = std::min<long>(chains, std::max(1, sh->sms * 3 / 10));
+    if (max_chain_ctas > 0) nc = std::min<long>(nc, max_chain_ctas);
     nc = std::max<long>(r, nc / r * r);
     if (nc + 8 > sh->sms) return false;
     sh->NC = (int)nc;
@@ -1257,18 +1260,19 @@ bool prefill_ring_supported(const PrefillArgs &a) {
     const long Ttot = a.cu_seqlens ? (long)a.T : (long)a.B * a.T;
     if (!(a.dtype == GDN_BF16 && a.dk == DK && a.dv == DV && a.chunk == C && Ttot > 0)) return false;
     RingShape sh;
-    return ring_shape(a, &sh);
+    return ring_shape(a, &sh, 0);
 }
 
-size_t prefill_ring_workspace(const PrefillArgs &a) {
+size_t prefill_ring_workspace(const PrefillArgs &a, int max_chain_ctas) {
     RingShape sh;
-    if (!ring_shape(a, &sh)) return 0;
+    if (!ring_shape(a, &sh, max_chain_ctas)) return 0;
     return ws_layout(a, sh).bytes;
 }
 
-cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStream_t s) {
+cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStream_t s,
+                                int max_chain_ctas) {
     RingShape sh;
-    if (!ring_shape(a, &sh)) return cudaErrorInvalidValue;
+    if (!ring_shape(a, &sh, max_chain_ctas)) return cudaErrorInvalidValue;
     const WsLayout L = ws_layout(a, sh);
     if (!ws || ws_bytes < L.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)) return cudaErrorInvalidValue;
     const long Ttot = a.cu_seqlens ? (long)a.T : (long)a.B * a.T;

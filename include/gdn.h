@@ -120,7 +120,7 @@ GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void 
  * The tensor-core prefill (dk = dv = 128, chunk 64, bf16) splits the GPU into CTAs that carry
  * the states and CTAs that prepare blocks for them, which hand each block's operands over
  * through a ring of slots in device memory; the workspace holds that ring (a fixed 96 KiB per
- * slot, 3 slots per state-carrying CTA) plus per-call tables that grow with B and Hv. It is
+ * slot, 16 slots per state-carrying CTA) plus per-call tables that grow with B and Hv. It is
  * scratch: nothing in it outlives a call. Host-only, no device work.
  */
 GDN_API size_t gdn_prefill_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, int chunk,
@@ -140,6 +140,38 @@ GDN_API int gdn_prefill_ws(const void *q, const void *k, const void *v, const vo
                            const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
                            int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype,
                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_prefill_static -- gdn_prefill that allocates no memory at call time.
+ *
+ * An addition of this library: the pages that define the operation have no counterpart of it.
+ * It is for callers that must not allocate device memory while they run, for instance a
+ * serving loop whose memory is fixed when it starts (cudaMalloc and cudaFree can synchronise
+ * the device and fail once memory is fragmented or taken) or a host framework that hands its
+ * kernels no workspace. Same arguments and result as gdn_prefill. The tensor-core path (dk =
+ * dv = 128, chunk 64, bf16, more than 8 tokens per sequence or cu_seqlens given) takes its
+ * scratch from one fixed 13 MiB array in the library's device image (one copy per device,
+ * present once the library's code is loaded there) and runs with at most 8 state-carrying
+ * CTAs, so it is slower than gdn_prefill on large batches; all other sizes run the same
+ * scratch-free kernels as gdn_prefill. Nothing is allocated: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *   Limit: the scratch holds the ring of 8 state-carrying CTAs (12 MiB) and 1 MiB of per-call
+ * tables, which take about 4*B*Hk + 8*B bytes plus 5 KiB (B up to about 14,000 at Hk = 16). A
+ * call whose sizes need more (that, or Hv/Hk > 8) returns GDN_ERR_UNSUPPORTED before anything
+ * is queued.
+ *   Set-up: the first call on each device, with that device current, looks up the scratch's
+ * device address (cudaGetSymbolAddress, which may load the library's device code on that
+ * device) and keeps it; make that first call before any stream capture. Every call clears
+ * the scratch's counters itself (in its first kernel), so no call depends on what an earlier
+ * one left there.
+ *   Races: all calls on one device share the one scratch. Calls whose work may overlap on the
+ * GPU (different streams without ordering between them, or several host threads) race on it
+ * and give wrong results; calls queued on one stream are ordered and safe.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_CUDA.
+ */
+GDN_API int gdn_prefill_static(const void *q, const void *k, const void *v, const void *g, const void *b,
+                               const float *state_in, float *state_out, void *out, const int32_t *cu_seqlens,
+                               int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int dtype, void *stream);
 
 /*
  * gdn_decode_step -- one recurrent step for N independent sequences.

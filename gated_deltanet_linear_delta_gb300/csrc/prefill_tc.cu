@@ -23,21 +23,28 @@
 // lanes: one thread owns one row of S in fp32 registers for the whole sequence,
 // and an fp16 copy of S is the A operand of the MMAs straight from TMEM.
 //
-// Work split (512 threads = two groups of 8 warps, two warps per scheduler):
-//   * threads 0..255, "prep", run one block ahead: TMA of the raw K, Q, V tiles,
-//     norms and gates, fp16 conversion, the Gram MMA, A and P, the blocked
-//     triangular solve on CUDA cores, W by MMA, then hands the block's operands
-//     over in one of two shared-memory stages;
-//   * threads 256..511, "chain", own the state (each thread half a row): per block two MMA round trips
-//     (U^T, then the state update) plus the output products.
-// Each group issues its own MMAs from one thread; stages are handed over with
-// mbarriers (full / empty), MMA completion is tracked with tcgen05.commit.
+// Work split: one thread-block cluster of P CTAs per value head (P = 4 when every head's
+// cluster fits on the GPU at once, else 2, else 1; 512 threads each). Rank 0 carries the state.
+//   * F = 0: every CTA prepares blocks (TMA of the raw K, Q, V tiles, norms and gates, fp16
+//     conversion, the Gram MMA, A and P, the blocked triangular solve on CUDA cores, W by MMA);
+//     helper ranks send their blocks' operands into the state CTA's shared memory by
+//     distributed-shared-memory bulk copies, and rank 0's own threads 0..255 prepare the rest.
+//     Threads 256..511 of rank 0 own the state (two threads per row) and issue its MMAs: per
+//     block two dependent MMA round trips (U^T, then the state update) plus the output products.
+//   * F = 1 (P >= 3): rank 0 prepares no blocks. Its K, Q, V tiles come by TMA and the helpers
+//     send only Tb (as bf16 hi + lo), P, W and the block scalars; one thread issues every MMA,
+//     256 threads hold the state, 128 write the outputs and 96 convert the Q rows.
+// Stages and sent slots are handed over with mbarriers (full / empty, local or cluster scope);
+// MMA completion is tracked with tcgen05.commit. The ring kernel (prefill_ring.cu) is the
+// default for these sizes; this one runs when GDN_PREFILL_KERNEL=cluster.
 //
-// Numerics: every MMA multiplies fp16 operands into fp32 accumulators. Each
-// operand is scaled by an exact power of two before rounding to fp16 (per block
-// for V, Tb, Tw, W and P from their maxima; per row of S and U in the chain, so
-// no cross-thread reduction), which keeps every value in fp16's normal range and
-// each product to about 2^-11 relative. Raw q/k are normalised before rounding.
+// Numerics: MMAs multiply fp16 operands into fp32 accumulators, except where raw bf16 tiles
+// (K, V) meet an operand that fp16 cannot carry exactly enough: there that operand (Tb, and U
+// diag(d rk) in the state update) is split into bf16 hi + lo (about 16 significant bits) and
+// both halves are multiplied. fp16 operands are scaled by an exact power of two before rounding
+// (per block for V, Tb, Tw, W and P from their maxima; per row of S and U in the chain), which
+// keeps every value in fp16's normal range and each product to about 2^-11 relative. Raw q/k
+// are normalised before rounding.
 //
 // Rows t >= L of a partial block get zero kh, qh, beta, d, so they contribute
 // nothing; their outputs are not stored.

@@ -102,6 +102,18 @@ def test_in_place_state():
     check(b, out, so)
 
 
+@pytest.mark.parametrize("dtype,dk,dv,chunk", [("f32", 64, 64, 32), ("bf16", 32, 128, 16)])
+def test_in_place_state_cuda_core_kernel(dtype, dk, dv, chunk):
+    """state_in == state_out on the CUDA-core block kernel (sizes the tensor-core kernels do not
+    take): each row is read before it is overwritten, so the aliased call equals the oracle."""
+    b = inputs.make_batch(B=3, T=130, Hk=2, Hv=4, dk=dk, dv=dv, dtype=dtype, chunk=chunk, seed=8,
+                          init_state=True)
+    assert gdn.gdn_prefill_path(b.B, b.T, b.Hk, b.Hv, dk, dv, chunk,
+                                gdn.GDN_F32 if dtype == "f32" else gdn.GDN_BF16) == 0
+    out, so = run_prefill(b, in_place=True)
+    check(b, out, so)
+
+
 def test_split_call_equals_one_call():
     """Carrying the state across two calls gives the one-call result (prompt fragments)."""
     b = inputs.make_batch(B=1, T=300, Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", chunk=64, seed=8,

@@ -442,8 +442,11 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                 const int st = s & 1;
                 const uint32_t sbst = sb + st * CH_STAGE;
                 if (!wait_bar(full + st, (s >> 1) & 1, budget)) { ok = false; break; }
-                // the slot's copy has landed: its producer may reuse the slot for step s + kSlots
-                st_release_gpu(p.w.consumed + 32 * i, s + 1);
+                // The slot's copy has landed (its reads are complete once the barrier phase has
+                // flipped), so its producer may reuse the slot for step s + kSlots. A relaxed store
+                // suffices and keeps this thread going: a release here would also wait for the MMAs
+                // still in flight (about 2k cycles on the state's critical path).
+                st_relaxed_gpu(p.w.consumed + 32 * i, s + 1);
                 if (s > 0 && !wait_bar(d2free, (s - 1) & 1, budget)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1

@@ -434,13 +434,20 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
         if (!ok) set_abort(p);
     } else if (tid == 32) {
         // ---------------- issuer: every MMA ----------------
+        // This thread shares its scheduler with two busy epilogue warps, so it issues as few
+        // instructions as it can: the loops are unrolled and every shared-memory descriptor is a
+        // per-stage base plus a constant (a descriptor's address field counts 16-byte units).
+        const uint64_t dN = desc_sw128(sb + RS_N, 16384, 1024), dZ = desc_sw128(sb + RS_Z, 8192, 1024);
+        const uint64_t dBH = desc_sw128(sb + RS_BH, 16, 1024), dBL = desc_sw128(sb + RS_BL, 16, 1024);
+        const uint64_t dEH = desc_sw128(sb + RS_EH, 8192, 1024), dEL = desc_sw128(sb + RS_EL, 8192, 1024);
+        const uint64_t dV = desc_sw128(sb + CH_V, 8192, 1024);
         int s = 0;
         bool ok = true;
         for (int pos = 0; pos < p.npos && ok; ++pos) {
             const int nb = fs[pos + 1] - fs[pos];
             for (int b = 0; b < nb; ++b, ++s) {
                 const int st = s & 1;
-                const uint32_t sbst = sb + st * CH_STAGE;
+                const uint64_t so = st ? (uint64_t)(CH_STAGE >> 4) : 0ull;  // stage offset in descriptor units
                 if (!wait_bar(full + st, (s >> 1) & 1, budget)) { ok = false; break; }
                 // The slot's copy has landed (its reads are complete once the barrier phase has
                 // flipped), so its producer may reuse the slot for step s + kSlots. A relaxed store
@@ -449,11 +456,11 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                 st_relaxed_gpu(p.w.consumed + 32 * i, s + 1);
                 if (s > 0 && !wait_bar(d2free, (s - 1) & 1, budget)) { ok = false; break; }
                 tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {  // V^T (B hi + B lo)
-                    const uint64_t a = desc_sw128(sbst + CH_V + ks * 2048, 8192, 1024);
-                    mma_bf16(tmem + CT_D2, a, desc_sw128(sbst + RS_BH + ks * 32, 16, 1024), ID_VB, ks > 0);
-                    mma_bf16(tmem + CT_D2, a, desc_sw128(sbst + RS_BL + ks * 32, 16, 1024), ID_VB, 1);
+                    const uint64_t a = dV + so + ks * (2048 >> 4);
+                    mma_bf16(tmem + CT_D2, a, dBH + so + ks * (32 >> 4), ID_VB, ks > 0);
+                    mma_bf16(tmem + CT_D2, a, dBL + so + ks * (32 >> 4), ID_VB, 1);
                 }
                 if (!wait_bar(s16, s & 1, budget)) { ok = false; break; }
                 tc_fence_after();
@@ -462,23 +469,21 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                 gam[s & 1] = gst[st];
                 mbar_arrive(scb + (s & 1));
                 const uint32_t a16 = tmem + CT_S16 + 64 * (s & 1);
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)  // S N: the state's dependent product
-                    mma_f16_ts(tmem + CT_D1, a16 + 8 * ks, desc_sw128(sbst + RS_N + ks * 2048, 16384, 1024), ID_SN,
-                               ks > 0);
+                    mma_f16_ts(tmem + CT_D1, a16 + 8 * ks, dN + so + ks * (2048 >> 4), ID_SN, ks > 0);
                 mma_commit(d1);
                 if (s > 0 && !wait_bar(o12free, (s - 1) & 1, budget)) { ok = false; break; }
                 tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {  // V^T (E hi + E lo)
-                    const uint64_t a = desc_sw128(sbst + CH_V + ks * 2048, 8192, 1024);
-                    mma_bf16(tmem + CT_O2, a, desc_sw128(sbst + RS_EH + ks * 2048, 8192, 1024), ID_VE, ks > 0);
-                    mma_bf16(tmem + CT_O2, a, desc_sw128(sbst + RS_EL + ks * 2048, 8192, 1024), ID_VE, 1);
+                    const uint64_t a = dV + so + ks * (2048 >> 4);
+                    mma_bf16(tmem + CT_O2, a, dEH + so + ks * (2048 >> 4), ID_VE, ks > 0);
+                    mma_bf16(tmem + CT_O2, a, dEL + so + ks * (2048 >> 4), ID_VE, 1);
                 }
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)  // S Z
-                    mma_f16_ts(tmem + CT_O1, a16 + 8 * ks, desc_sw128(sbst + RS_Z + ks * 2048, 8192, 1024), ID_SZ,
-                               ks > 0);
+                    mma_f16_ts(tmem + CT_O1, a16 + 8 * ks, dZ + so + ks * (2048 >> 4), ID_SZ, ks > 0);
                 mma_commit(o1);
                 mma_commit(freeb + st);
             }
@@ -516,9 +521,10 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
         };
         // fp16 copy of S (row scale shared by the two halves) into TMEM buffer `buf`; false to leave
         auto publish_s16 = [&](int par, int buf, bool good) {
-            float mx = 0.f;
+            float m4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial maxima: a short dependent chain
 #pragma unroll
-            for (int e = 0; e < 64; ++e) mx = fmaxf(mx, fabsf(S[e]));
+            for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], fabsf(S[e]));
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             xch[(par * 2 + hf) * 128 + r] = good ? (int8_t)max(-127, row_exp(mx)) : (int8_t)127;
             bar_sync(pair_bar, 64);
             const int eo = xch[(par * 2 + (hf ^ 1)) * 128 + r];

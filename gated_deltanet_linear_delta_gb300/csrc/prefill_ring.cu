@@ -1231,9 +1231,11 @@ bool ring_shape(const PrefillArgs &a, RingShape *sh, int max_chain_ctas) {
     if (cudaDeviceGetAttribute(&sh->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     const int r = a.Hv / a.Hk;
     const long chains = (long)a.B * a.Hv;
-    // about a third of the SMs carry states; the rest prepare blocks. A multiple of r, so that the
-    // value heads of one key head sit in consecutive chain CTAs at the same steps.
-    long nc = std::min<long>(chains, std::max(1, sh->sms * 3 / 10));
+    // A quarter of the SMs carry states; the rest prepare blocks (measured on 16 packed sequences:
+    // 25% beats 20% and 30-40%; a single sequence needs one CTA per head, which 25% covers for 32
+    // heads). A multiple of r, so that the value heads of one key head sit in consecutive chain
+    // CTAs at the same steps.
+    long nc = std::min<long>(chains, std::max(1, sh->sms / 4));
     if (max_chain_ctas > 0) nc = std::min<long>(nc, max_chain_ctas);
     nc = std::max<long>(r, nc / r * r);
     if (nc + 8 > sh->sms) return false;

@@ -92,7 +92,10 @@ typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
  *   B, T          : sequence count; tokens per sequence (cu_seqlens NULL) or
  *                   total packed tokens (cu_seqlens given).
  *   Hk, Hv, dk, dv: head counts and head dimensions; dk, dv in {32, 64, 128}.
- *   chunk         : block length, one of 16, 32, 64.
+ *   chunk         : block length, one of 16, 32, 64. The tensor-core kernels take bf16 with
+ *                   dk = dv = 128 and chunk 64; every other supported combination (chunk 16
+ *                   or 32, fp32, dk or dv of 32 or 64) runs a CUDA-core block kernel that is
+ *                   correct but is not a performance path (gdn_prefill_path returns 0 for it).
  * Sequences of at most 8 tokens each (cu_seqlens NULL, T <= 8: a few tokens
  * per sequence, e.g. checking a run of speculated tokens) are evaluated as a
  * token scan instead: every state row is read once, takes the T updates in

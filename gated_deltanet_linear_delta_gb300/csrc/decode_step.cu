@@ -30,8 +30,12 @@
 // A negative slot marks a padding row (state untouched, output zero); a slot
 // >= num_slots is a caller error, flagged on the device status word and
 // skipped the same way.
+#include <algorithm>
+#include <atomic>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "tc_ops.cuh"
 
 namespace gdn {
 namespace {
@@ -124,127 +128,179 @@ decode_step_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const T
 // A few tokens per sequence (1 <= T <= kScanMaxT), the shape of checking a short run of
 // speculated tokens: each state row is read once from state_in (or zero), all T tokens
 // are applied in order while it sits in registers, and it is written once to state_out
-// (which may be state_in: each lane reads its pieces of a row before it writes them). The
-// T steps cost one pass over the state instead of T.
+// (which may be state_in). The T steps cost one pass over the state instead of T.
 //
-// The key and query norms of a token are the same for every row of a head, so each CTA
-// computes them once (one warp per token) into shared memory before the scan.
+// The CTAs are persistent and take one (sequence, value head) state at a time: its rows are
+// spread over the CTA's 8 warps (8 lanes per row), and while they are updated in registers
+// the next head's state is already on its way into shared memory (one bulk copy), so the
+// HBM reads of one head overlap the arithmetic of the previous one.
 //
-// Since every token adds two dot products per row, the row is spread over only
-// kScanLanes = 8 lanes (DK/32 float4 pieces each, interleaved so that the 8 lanes read
-// 128 contiguous bytes at a time): a 3-step shuffle reduction then serves the 4 rows of a
-// warp pass at once, where 32 lanes per row would take 5 steps for one row.
+// Everything a token contributes that is the same for every row of a head -- the normalised
+// key and query (fp32), v, alpha, beta and kh . qh -- is computed once per head into shared
+// memory (one warp per token), so the per-row work of a token is two dot products, one
+// paired reduction and the update. Each lane holds DK/32 float4 pieces of its row,
+// interleaved so that the 8 lanes of a row read 128 contiguous bytes at a time. The two
+// reductions of a row share one 3-step shuffle tree: at the first step each lane keeps one
+// of the two sums and sends the other, so every step moves one value.
 constexpr int kScanLanes = 8;
-constexpr int kScanPasses = 2;
+constexpr int kScanWarps = kDecodeThreads / 32;
+constexpr long long kScanWait = 4000000000LL;  // SM cycles before a wait for a state copy gives up
+
+template <int DK, int DV>
+struct ScanSmem {
+    float4 state[DV * DK / 4];          // the next head's state (bulk copy)
+    float4 kq[kScanMaxT][2][DK / 4];    // per token: kh, qh (normalised)
+    float v[kScanMaxT][DV];             // per token: v
+    float sc[kScanMaxT][4];             // per token: alpha, beta, kh . qh
+    uint64_t bar;
+};
 
 template <int DK, int DV, typename TIn>
-__global__ void __launch_bounds__(kDecodeThreads, 3)
+__global__ void __launch_bounds__(kDecodeThreads, 2)
 scan_tokens_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
                    const TIn *__restrict__ g, const TIn *__restrict__ b, const float *state_in,
-                   float *state_out, TIn *__restrict__ out, int B, int T, int Hk, int Hv) {
+                   float *state_out, TIn *__restrict__ out, int B, int T, int Hk, int Hv, int *status) {
     constexpr int LPR = kScanLanes;
     constexpr int CPL = DK / (4 * LPR);  // float4 pieces per lane
     constexpr int RPW = 32 / LPR;        // rows per warp pass
-    constexpr int R = kScanPasses;
-    constexpr int ROWS_PER_WARP = RPW * R;
-    static_assert(CPL >= 1 && DV % ROWS_PER_WARP == 0, "a warp must stay within one head");
+    constexpr int R = DV / (RPW * kScanWarps);  // passes: the CTA's warps cover the DV rows of a head
+    static_assert(CPL >= 1 && R >= 1 && R * RPW * kScanWarps == DV, "the CTA must cover one head");
+    static_assert(LPR == 8, "the paired reduction below is a 3-step tree");
+    constexpr uint32_t kStateBytes = DV * DK * 4;
 
-    // warps of this CTA that share a head (a CTA holds one head, or two when DV = 32)
-    constexpr int GW = DV / ROWS_PER_WARP < kDecodeThreads / 32 ? DV / ROWS_PER_WARP : kDecodeThreads / 32;
-    __shared__ float s_nrm[kDecodeThreads / 32 / GW][kScanMaxT][3];  // per head and token: rk, rq, k.q
-
+    extern __shared__ __align__(128) uint8_t scan_smem_raw[];
+    ScanSmem<DK, DV> &sm = *reinterpret_cast<ScanSmem<DK, DV> *>(scan_smem_raw);
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const long warp = (long)blockIdx.x * (kDecodeThreads / 32) + wib;
-    const long row0 = warp * ROWS_PER_WARP;
-    const bool valid = row0 < (long)B * Hv * DV;
-    const long nh = row0 / DV;
-    const int i0 = (int)(row0 % DV);
-    const int h = (int)(nh % Hv);
-    const long n = nh / Hv;
-    const int hk = h / (Hv / Hk);
     const int grp = lane / LPR;  // row within a pass
     const int c = lane % LPR;    // piece j of this lane covers columns 4 (c + LPR j) .. +3
+    const long heads = (long)B * Hv;
+    const bool low = (c & 4) == 0;  // after the first reduction step: low lanes hold S.kh, high lanes S.qh
 
-    float4 s[R][CPL];
-    if (valid) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const long off = (nh * DV + i0 + r * RPW + grp) * (long)DK;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j)
-                s[r][j] = state_in ? __ldcs(reinterpret_cast<const float4 *>(state_in + off + 4 * (c + LPR * j)))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        // the norms of this head's tokens, once per CTA: warp w of the head takes tokens w, w + GW, ...
-        for (int t = wib % GW; t < T; t += GW) {
-            const long kq_off = ((n * T + t) * Hk + hk) * (long)DK;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&sm.bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    long nh = blockIdx.x;
+    if (threadIdx.x == 0 && state_in && nh < heads) {
+        tc::mbar_expect_tx(&sm.bar, kStateBytes);
+        tc::bulk_load(sm.state, state_in + nh * (long)(DV * DK), kStateBytes, &sm.bar);
+    }
+    for (uint32_t it = 0; nh < heads; ++it, nh += gridDim.x) {
+        const int h = (int)(nh % Hv);
+        const long n = nh / Hv;
+        const int hk = h / (Hv / Hk);
+        // this head's tokens: warp w takes tokens w, w + 8, ...
+        for (int t = wib; t < T; t += kScanWarps) {
+            const long tok = n * T + t;
+            const long kq_off = (tok * Hk + hk) * (long)DK;
+            float kx[DK / 32], qx[DK / 32];
             float pkk = 0.f, pqq = 0.f, pkq = 0.f;
 #pragma unroll
             for (int j = 0; j < DK / 32; ++j) {
-                const float kx = to_f32(k[kq_off + lane + 32 * j]), qx = to_f32(q[kq_off + lane + 32 * j]);
-                pkk += kx * kx;
-                pqq += qx * qx;
-                pkq += kx * qx;
+                kx[j] = to_f32(k[kq_off + lane + 32 * j]);
+                qx[j] = to_f32(q[kq_off + lane + 32 * j]);
+                pkk += kx[j] * kx[j];
+                pqq += qx[j] * qx[j];
+                pkq += kx[j] * qx[j];
             }
             pkk = warp_sum(pkk);
             pqq = warp_sum(pqq);
             pkq = warp_sum(pkq);
+            const float rk = rsqrtf(pkk + kNormEps), rq = rsqrtf(pqq + kNormEps);
+            float *kh = reinterpret_cast<float *>(sm.kq[t][0]), *qh = reinterpret_cast<float *>(sm.kq[t][1]);
+#pragma unroll
+            for (int j = 0; j < DK / 32; ++j) {
+                kh[lane + 32 * j] = kx[j] * rk;
+                qh[lane + 32 * j] = qx[j] * rq;
+            }
+#pragma unroll
+            for (int j = 0; j < (DV + 31) / 32; ++j)
+                if (lane + 32 * j < DV) sm.v[t][lane + 32 * j] = to_f32(v[(tok * Hv + h) * DV + lane + 32 * j]);
             if (lane == 0) {
-                s_nrm[wib / GW][t][0] = rsqrtf(pkk + kNormEps);
-                s_nrm[wib / GW][t][1] = rsqrtf(pqq + kNormEps);
-                s_nrm[wib / GW][t][2] = pkq;
+                sm.sc[t][0] = expf(to_f32(g[tok * Hv + h]));
+                sm.sc[t][1] = sigmoidf_(to_f32(b[tok * Hv + h]));
+                sm.sc[t][2] = pkq * rk * rq;
             }
         }
-    }
-    __syncthreads();
-    if (!valid) return;
-#pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-        const long tok = n * T + t;
-        const long kq_off = (tok * Hk + hk) * (long)DK;
-        float4 kh[CPL], qh[CPL];
+        // the state of this head: from the bulk copy (or zero)
+        bool failed = false;
+        if (state_in) failed = !tc::mbar_wait(&sm.bar, it & 1, kScanWait);
+        float4 s[R][CPL];
+        const int rbase = wib * (R * RPW) + grp;  // row of pass r: rbase + r * RPW
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            kh[j] = load4(k + kq_off + 4 * (c + LPR * j));
-            qh[j] = load4(q + kq_off + 4 * (c + LPR * j));
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int j = 0; j < CPL; ++j)
+                s[r][j] = state_in ? sm.state[(rbase + r * RPW) * (DK / 4) + c + LPR * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        // every thread has read the buffer (and the token values are visible): the next head's copy may start
+        if (__syncthreads_or(failed)) {
+            if (threadIdx.x == 0) {
+                flag_error(status);
+                tc::mbar_wait(&sm.bar, it & 1, kScanWait);  // the copy must land before the CTA leaves
+            }
+            return;
         }
-        float vi[R];
+        if (threadIdx.x == 0 && state_in && nh + gridDim.x < heads) {
+            tc::fence_async_smem();
+            tc::mbar_expect_tx(&sm.bar, kStateBytes);
+            tc::bulk_load(sm.state, state_in + (nh + gridDim.x) * (long)(DV * DK), kStateBytes, &sm.bar);
+        }
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            const float alpha = sm.sc[t][0], beta = sm.sc[t][1], kq = sm.sc[t][2];
+            float4 kh[CPL], qh[CPL];
 #pragma unroll
-        for (int r = 0; r < R; ++r) vi[r] = to_f32(v[(tok * Hv + h) * DV + i0 + r * RPW + grp]);
-        const float alpha = expf(to_f32(g[tok * Hv + h]));
-        const float beta = sigmoidf_(to_f32(b[tok * Hv + h]));
-        const float rk = s_nrm[wib / GW][t][0], rq = s_nrm[wib / GW][t][1];
-        const float kq = s_nrm[wib / GW][t][2] * rk * rq;
+            for (int j = 0; j < CPL; ++j) {
+                kh[j] = sm.kq[t][0][c + LPR * j];
+                qh[j] = sm.kq[t][1][c + LPR * j];
+            }
+            const long orow = ((n * T + t) * Hv + h) * DV;
+            // the R rows are independent: each stage below runs over all of them, so their
+            // dependent chains (dots, shuffle steps, update) interleave
+            float x[R], send[R];
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            kh[j] = make_float4(kh[j].x * rk, kh[j].y * rk, kh[j].z * rk, kh[j].w * rk);
-            qh[j] = make_float4(qh[j].x * rq, qh[j].y * rq, qh[j].z * rq, qh[j].w * rq);
+            for (int r = 0; r < R; ++r) {
+                float pk2[2] = {0.f, 0.f}, pq2[2] = {0.f, 0.f};  // two chains each: shorter dependences
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    pk2[j & 1] += dot4(s[r][j], kh[j]);
+                    pq2[j & 1] += dot4(s[r][j], qh[j]);
+                }
+                const float psk = pk2[0] + pk2[1], psq = pq2[0] + pq2[1];
+                x[r] = low ? psk : psq;  // paired reduction over the row's 8 lanes: keep one sum, send the other
+                send[r] = low ? psq : psk;
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) x[r] += __shfl_xor_sync(0xffffffffu, send[r], 4);
+#pragma unroll
+            for (int r = 0; r < R; ++r) x[r] += __shfl_xor_sync(0xffffffffu, x[r], 2);
+#pragma unroll
+            for (int r = 0; r < R; ++r) x[r] += __shfl_xor_sync(0xffffffffu, x[r], 1);
+#pragma unroll
+            for (int r = 0; r < R; ++r) send[r] = __shfl_xor_sync(0xffffffffu, x[r], 4);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float sk = low ? x[r] : send[r], sq = low ? send[r] : x[r];
+                const int row = rbase + r * RPW;
+                const float u = beta * (sm.v[t][row] - alpha * sk);
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    s[r][j].x = fmaf(alpha, s[r][j].x, u * kh[j].x);
+                    s[r][j].y = fmaf(alpha, s[r][j].y, u * kh[j].y);
+                    s[r][j].z = fmaf(alpha, s[r][j].z, u * kh[j].z);
+                    s[r][j].w = fmaf(alpha, s[r][j].w, u * kh[j].w);
+                }
+                if (c == 0) out[orow + row] = from_f32<TIn>(fmaf(alpha, sq, u * kq));
+            }
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            float psk = 0.f, psq = 0.f;
+            const long off = (nh * DV + rbase + r * RPW) * (long)DK;
 #pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                psk += dot4(s[r][j], kh[j]);
-                psq += dot4(s[r][j], qh[j]);
-            }
-            const float sk = group_sum<LPR>(psk), sq = group_sum<LPR>(psq);
-            const float u = beta * (vi[r] - alpha * sk);
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                s[r][j].x = alpha * s[r][j].x + u * kh[j].x;
-                s[r][j].y = alpha * s[r][j].y + u * kh[j].y;
-                s[r][j].z = alpha * s[r][j].z + u * kh[j].z;
-                s[r][j].w = alpha * s[r][j].w + u * kh[j].w;
-            }
-            if (c == 0) out[(tok * Hv + h) * DV + i0 + r * RPW + grp] = from_f32<TIn>(alpha * sq + u * kq);
+            for (int j = 0; j < CPL; ++j) __stcs(reinterpret_cast<float4 *>(state_out + off + 4 * (c + LPR * j)), s[r][j]);
         }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const long off = (nh * DV + i0 + r * RPW + grp) * (long)DK;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) __stcs(reinterpret_cast<float4 *>(state_out + off + 4 * (c + LPR * j)), s[r][j]);
+        __syncthreads();  // the token values of this head are read before the next head's overwrite them
     }
 }
 
@@ -275,14 +331,29 @@ cudaError_t dispatch_dims(const DecodeArgs &a, cudaStream_t s) {
 
 template <int DK, int DV, typename TIn>
 cudaError_t launch_scan_t(const PrefillArgs &a, cudaStream_t s) {
-    constexpr int ROWS_PER_WARP = (32 / kScanLanes) * kScanPasses;
-    const long rows = (long)a.B * a.Hv * DV;
-    const long warps = (rows + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
-    const long blocks = (warps + kDecodeThreads / 32 - 1) / (kDecodeThreads / 32);
-    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    scan_tokens_kernel<DK, DV, TIn><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(
+    const long heads = (long)a.B * a.Hv;
+    constexpr int kBytes = (int)sizeof(ScanSmem<DK, DV>);
+    const auto kern = scan_tokens_kernel<DK, DV, TIn>;
+    // resident CTAs per device for this instantiation, found once per device (0: not yet)
+    static std::atomic<int> resident[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int ctas = resident[dev].load(std::memory_order_relaxed);
+    if (ctas == 0) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, kBytes);
+        if (e != cudaSuccess) return e;
+        ctas = sms * std::max(per_sm, 1);
+        resident[dev].store(ctas, std::memory_order_relaxed);
+    }
+    const long blocks = std::min<long>(heads, (long)ctas);
+    kern<<<(unsigned)blocks, kDecodeThreads, kBytes, s>>>(
         (const TIn *)a.q, (const TIn *)a.k, (const TIn *)a.v, (const TIn *)a.g, (const TIn *)a.b,
-        a.state_in, a.state_out, (TIn *)a.out, a.B, a.T, a.Hk, a.Hv);
+        a.state_in, a.state_out, (TIn *)a.out, a.B, a.T, a.Hk, a.Hv, a.status);
     return cudaGetLastError();
 }
 

@@ -298,6 +298,16 @@ __device__ void solve128(const float *sA, float *sT, int p, int bar_id) {
     }
 }
 
+// Chain id of list position `pos` of chain CTA (group m, member v). Chains are numbered
+// (sequence rank, key head, member) with sequences longest first; position pos hands the G
+// groups the next G (sequence, key head) items, left to right at even positions and right to
+// left at odd ones, so that a group that took a longer item at one position takes a shorter
+// one at the next (serpentine order: the groups' total steps stay close).
+__device__ __forceinline__ long chain_id(const RingParams &p, int m, int v, int pos) {
+    const int mm = (pos & 1) ? p.G - 1 - m : m;
+    return ((long)pos * p.G + mm) * p.r + v;
+}
+
 // ---- the plan: sequence order, block counts, step tables; counters zeroed ----
 __global__ void __launch_bounds__(1024) ring_plan_kernel(const RingParams p) {
     __shared__ int s_len[kRankMax];
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(1024) ring_plan_kernel(const RingParams p) {
         int *fs = p.w.first_step + (long)m * (p.npos + 1);
         for (int pos = 0; pos < p.npos; ++pos) {
             fs[pos] = acc;
-            const long c = (long)m * p.r + (long)pos * p.NC;
+            const long c = chain_id(p, m, 0, pos);
             if (c < nchains) acc += p.w.nblk[p.w.seq_rank[c / p.Hv]];
         }
         fs[p.npos] = acc;
@@ -354,10 +364,6 @@ __global__ void __launch_bounds__(1024) ring_plan_kernel(const RingParams p) {
     }
 }
 
-// chain id of list position `pos` of chain CTA (group m, member v)
-__device__ __forceinline__ long chain_id(const RingParams &p, int m, int v, int pos) {
-    return (long)m * p.r + v + (long)pos * p.NC;
-}
 
 struct ChainInfo {
     int n, h, nb;

@@ -74,6 +74,10 @@ constexpr uint32_t RS_BL = 65536;   //   16 KiB B^T lo
 constexpr uint32_t RS_EH = 81920;   //    8 KiB E hi, MN-major [t 0..63][s 0..63]
 constexpr uint32_t RS_EL = 90112;   //    8 KiB E lo
 constexpr uint32_t RS_BYTES = 98304;
+constexpr uint32_t RS_HEAD = RS_EH;  // a stage is loaded in two parts: [0, RS_HEAD) and the E images
+// Once a step's MMAs are done, its stage's E region (16 KiB) holds that step's bf16 outputs,
+// [dv block 0..1][t][128 B] with the 128-byte swizzle, for one tensor store per dv block.
+constexpr uint32_t CH_OUT = RS_EH;
 static_assert((size_t)kStaticChainCtas * kSlots * RS_BYTES + ((size_t)1 << 20) <= kStaticScratchBytes,
               "the fixed scratch holds the ring of its chain CTAs plus 1 MiB of tables");
 
@@ -81,7 +85,7 @@ static_assert((size_t)kStaticChainCtas * kSlots * RS_BYTES + ((size_t)1 << 20) <
 constexpr uint32_t CH_V = RS_BYTES;                  // raw V tile [i-block 0..1][t][128 B], 16 KiB
 constexpr uint32_t CH_STAGE = RS_BYTES + 16384;      // two stages
 constexpr uint32_t CH_XCH = 2 * CH_STAGE;            // [2 parities][2 halves][128 rows] int8 row exponents
-constexpr uint32_t CH_SC = CH_XCH + 512;             // [2] gamma of the step (written by the issuer)
+constexpr uint32_t CH_SC = CH_XCH + 512;             // gamma [2] of the step, [2] of the stage; staged-output info [2][4]
 constexpr uint32_t CH_BAR = CH_SC + 64;
 constexpr uint32_t CH_END = CH_BAR + 256;
 static_assert(CH_STAGE % 1024 == 0 && CH_V % 1024 == 0, "chain stages need 1 KiB alignment");
@@ -389,7 +393,8 @@ __device__ __forceinline__ uint8_t *ring_slot(const RingParams &p, int i, int s)
 }
 
 // ======================= chain CTA =======================
-__device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t *sm, uint32_t sb, uint32_t tmem) {
+__device__ void chain_cta(const CUtensorMap *tm_v, const CUtensorMap *tm_o, const RingParams &p, uint8_t *sm,
+                          uint32_t sb, uint32_t tmem) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i = blockIdx.x, m = i / p.r, v = i % p.r;
     const int *fs = p.w.first_step + (long)m * (p.npos + 1);
@@ -397,15 +402,37 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + CH_BAR);
     uint64_t *full = bars + 0, *freeb = bars + 2, *d1 = bars + 4, *o1 = bars + 5, *s16 = bars + 6,
              *d2free = bars + 7, *o12free = bars + 8, *scb = bars + 9, *fin = bars + 11;
+    uint64_t *fulle = bars + 12;    // [2] the stage's E images landed
+    uint64_t *ostaged = bars + 14;  // [2] the step's outputs staged in the stage's E region (256 arrivals)
+    // [2][4] per stage: 1 if the staged outputs are to be stored (a full block), their first token, head
+    int *oinfo = reinterpret_cast<int *>(sm + CH_SC + 16);
     float *gam = reinterpret_cast<float *>(sm + CH_SC);  // [2] gamma of step s at [s & 1], for the epilogue
     float *gst = gam + 2;                                 // [2] gamma of the block in stage st
     const long long budget = p.wait_budget;
 
     if (tid == 0) {
-        // ---------------- loader: ring slot (bulk copy) + raw V tile (TMA) per step ----------------
+        // ---------------- loader: ring slot (bulk copies) + raw V tile (TMA) per step ----------------
+        // A stage is refilled in two parts: everything but the E images as soon as the step two
+        // before is done, then -- once the outputs that step staged in the E region have been
+        // read out by their tensor store -- the E images, which are needed last.
         prefetch_tmap(tm_v);
+        prefetch_tmap(tm_o);
         int s = 0, issued = 0;
         bool ok = true;
+        // tensor store of the outputs step j staged (if it was a full block); false when the wait ran out
+        auto store_outputs = [&](int j, long long lim) {
+            const int sj = j & 1;
+            if (!wait_bar(ostaged + sj, (j >> 1) & 1, lim)) return false;
+            if (oinfo[4 * sj]) {
+                const int tok = oinfo[4 * sj + 1], hh = oinfo[4 * sj + 2];
+                tma_store_3d(tm_o, sm + sj * CH_STAGE + CH_OUT, 0, hh, tok);
+                tma_store_3d(tm_o, sm + sj * CH_STAGE + CH_OUT + 8192, 64, hh, tok);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+            return true;
+        };
+        int e_issued = 0;
         for (int pos = 0; pos < p.npos && ok; ++pos) {
             const int nb = fs[pos + 1] - fs[pos];
             if (nb == 0) continue;
@@ -425,18 +452,28 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                 uint8_t *stage = sm + st * CH_STAGE;
                 // the block's gamma, read before the slot can be rewritten (that waits for `consumed`)
                 gst[st] = p.w.slot_sc[((long)i * kSlots + s % kSlots) * 4];
-                mbar_expect_tx(full + st, RS_BYTES + 16384);
-                bulk_load(stage, ring_slot(p, i, s), RS_BYTES, full + st);
+                mbar_expect_tx(full + st, RS_HEAD + 16384);
+                bulk_load(stage, ring_slot(p, i, s), RS_HEAD, full + st);
                 const int tok = (int)(ci.bos + (long)b * C);
                 tma_load_3d(stage + CH_V, tm_v, 0, ci.h, tok, full + st);
                 tma_load_3d(stage + CH_V + 8192, tm_v, 64, ci.h, tok, full + st);
                 issued = s + 1;
+                if (s >= 2 && !store_outputs(s - 2, budget)) { ok = false; break; }
+                mbar_expect_tx(fulle + st, RS_BYTES - RS_HEAD);
+                bulk_load(stage + RS_HEAD, ring_slot(p, i, s) + RS_HEAD, RS_BYTES - RS_HEAD, fulle + st);
+                e_issued = s + 1;
             }
         }
+        // the last two steps' outputs (after a failure: whatever was staged, within a bounded wait)
+        for (int j = max(0, issued - 2); j < issued; ++j)
+            if (!store_outputs(j, ok ? budget : kDrainBudget / 8)) ok = false;
+        bulk_wait_all();
         // copies still landing must land before the CTA leaves (after a failure: the issuer may
         // have stopped waiting for them)
         for (int j = issued - 2; j < issued; ++j)
             if (j >= 0) wait_bar(full + (j & 1), (j >> 1) & 1, kDrainBudget);
+        for (int j = e_issued - 2; j < e_issued; ++j)
+            if (j >= 0) wait_bar(fulle + (j & 1), (j >> 1) & 1, kDrainBudget);
         if (!ok) set_abort(p);
     } else if (tid == 32) {
         // ---------------- issuer: every MMA ----------------
@@ -455,11 +492,6 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                 const int st = s & 1;
                 const uint64_t so = st ? (uint64_t)(CH_STAGE >> 4) : 0ull;  // stage offset in descriptor units
                 if (!wait_bar(full + st, (s >> 1) & 1, budget)) { ok = false; break; }
-                // The slot's copy has landed (its reads are complete once the barrier phase has
-                // flipped), so its producer may reuse the slot for step s + kSlots. A relaxed store
-                // suffices and keeps this thread going: a release here would also wait for the MMAs
-                // still in flight (about 2k cycles on the state's critical path).
-                st_relaxed_gpu(p.w.consumed + 32 * i, s + 1);
                 if (s > 0 && !wait_bar(d2free, (s - 1) & 1, budget)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -480,6 +512,12 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                     mma_f16_ts(tmem + CT_D1, a16 + 8 * ks, dN + so + ks * (2048 >> 4), ID_SN, ks > 0);
                 mma_commit(d1);
                 if (s > 0 && !wait_bar(o12free, (s - 1) & 1, budget)) { ok = false; break; }
+                if (!wait_bar(fulle + st, (s >> 1) & 1, budget)) { ok = false; break; }
+                // Both copies of the slot have landed (their reads are complete once the barrier
+                // phases have flipped), so its producer may reuse the slot for step s + kSlots. A
+                // relaxed store suffices and keeps this thread going: a release here would also wait
+                // for the MMAs still in flight (about 2k cycles per step).
+                st_relaxed_gpu(p.w.consumed + 32 * i, s + 1);
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {  // V^T (E hi + E lo)
@@ -601,6 +639,7 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                 // outputs of this step
                 const bool good_o = __all_sync(0xffffffffu, good && wait_bar(o1, s & 1, budget));
                 tc_fence_after();
+                const int so = s & 1;
                 if (good_o) {
                     uint32_t a[32], c2[32];
                     tmem_ld32_nw(tmem + lane_off + CT_O1 + 32 * hf, a);
@@ -608,17 +647,37 @@ __device__ void chain_cta(const CUtensorMap *tm_v, const RingParams &p, uint8_t 
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(o12free);
-                    __nv_bfloat16 *op = p.out + ((ci.bos + (long)b * C + 32 * hf) * p.Hv + ci.h) * DV + r;
-                    const long tstride = (long)p.Hv * DV;
+                    if (L == C) {  // a full block: into the stage's E region, for one tensor store per dv block
+                        uint8_t *ob = sm + so * CH_STAGE + CH_OUT + (r >> 6) * 8192 + ((r & 7) << 1);
+                        const int ch = (r & 63) >> 3;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (32 * hf + e < L)
-                            op[e * tstride] = __float2bfloat16_rn(
-                                fmaf(srow_step, __uint_as_float(a[e]), __uint_as_float(c2[e])));
+                        for (int e = 0; e < 32; ++e) {
+                            const int t = 32 * hf + e;
+                            *reinterpret_cast<__nv_bfloat16 *>(ob + t * 128 + ((ch ^ (t & 7)) << 4)) =
+                                __float2bfloat16_rn(fmaf(srow_step, __uint_as_float(a[e]), __uint_as_float(c2[e])));
+                        }
+                        fence_async_smem();
+                        if (r == 0 && hf == 0) {
+                            oinfo[4 * so] = 1;
+                            oinfo[4 * so + 1] = (int)(ci.bos + (long)b * C);
+                            oinfo[4 * so + 2] = ci.h;
+                        }
+                    } else {  // a partial block: only its L rows, straight to global memory
+                        __nv_bfloat16 *op = p.out + ((ci.bos + (long)b * C + 32 * hf) * p.Hv + ci.h) * DV + r;
+                        const long tstride = (long)p.Hv * DV;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (32 * hf + e < L)
+                                op[e * tstride] = __float2bfloat16_rn(
+                                    fmaf(srow_step, __uint_as_float(a[e]), __uint_as_float(c2[e])));
+                        if (r == 0 && hf == 0) oinfo[4 * so] = 0;
+                    }
                 } else {
                     tc_fence_before();
                     mbar_arrive(o12free);
+                    if (r == 0 && hf == 0) oinfo[4 * so] = 0;
                 }
+                mbar_arrive(ostaged + so);
                 if (!good || !good_o) { ok = false; break; }
                 if (last) {  // (the loop's own increment of s is skipped by the break)
                     pos = npos_;
@@ -1150,7 +1209,8 @@ __device__ void prep_cta(const CUtensorMap *tm_q, const CUtensorMap *tm_k, const
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_ring_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const RingParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const RingParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -1170,6 +1230,10 @@ prefill_ring_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mbar_init(bars + 9, 1);                                    // scb[2]
             mbar_init(bars + 10, 1);
             mbar_init(bars + 11, 1);                                   // fin
+            mbar_init(bars + 12, 1);                                   // fulle[2]
+            mbar_init(bars + 13, 1);
+            mbar_init(bars + 14, 256);                                 // ostaged[2]
+            mbar_init(bars + 15, 256);
         } else {
             for (int pipe = 0; pipe < 2; ++pipe) {
                 uint64_t *pb = reinterpret_cast<uint64_t *>(sm + pipe * PP_BYTES + PP_BAR);
@@ -1185,7 +1249,7 @@ prefill_ring_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (chain)
-        chain_cta(&tm_v, p, sm, sb, tmem);
+        chain_cta(&tm_v, &tm_o, p, sm, sb, tmem);
     else
         prep_cta(&tm_q, &tm_k, p, sm, sb, tmem);
     tc_fence_before();
@@ -1293,9 +1357,9 @@ cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes,
     const WsLayout L = ws_layout(a, sh);
     if (!ws || ws_bytes < L.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)) return cudaErrorInvalidValue;
     const long Ttot = a.cu_seqlens ? (long)a.T : (long)a.B * a.T;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.q, DK, a.Hk, Ttot) || !make_map(&mk, a.k, DK, a.Hk, Ttot) ||
-        !make_map(&mv, a.v, DV, a.Hv, Ttot))
+        !make_map(&mv, a.v, DV, a.Hv, Ttot) || !make_map(&mo, a.out, DV, a.Hv, Ttot))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(prefill_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
@@ -1345,7 +1409,7 @@ cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes,
     cfg.stream = s;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_ring_kernel, mq, mk, mv, p);
+    return cudaLaunchKernelEx(&cfg, prefill_ring_kernel, mq, mk, mv, mo, p);
 }
 
 }  // namespace gdn

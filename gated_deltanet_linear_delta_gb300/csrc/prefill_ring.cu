@@ -121,7 +121,7 @@ constexpr int PS_DRK = 576;    // d_s rk_s                  (Tb' rows, W^T d col
 constexpr int PS_ER = 640;     // e_t rq_t                   (Qt rows)
 constexpr int PS_MISC = 704;   // gmin, gmax, factor flag, gamma, 1 / sigma
 constexpr int PS_RED = 720;    // [4 warps] reductions
-constexpr int PS_UNIT = 736;   // int[16]: the unit record
+constexpr int PS_UNIT = 768;   // int[2][16]: unit records, unit h in [h & 1]
 constexpr int PS_MAIL = 752;   // int[4]: to the publisher: [0] ring CTA (-1: stop), [1] step, [2] gamma bits, [3] failed
 // unit record (int offsets)
 constexpr int U_VALID = 0, U_S = 1, U_RI = 2, U_H = 3, U_HK = 4, U_TOK = 5, U_L = 6;
@@ -754,16 +754,21 @@ __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
     int tma_pending = 0;
     prefetch_tmap(tm_q);
     prefetch_tmap(tm_k);
-    for (uint32_t h = 0; ok; ++h) {
-        int *rec = P.pu;
+    // next unit with work into rec (rec[U_VALID] = 0: none left)
+    auto grab = [&](int *rec) {
         bool any = false;
-        while (!any) {  // next unit with work (or none)
+        while (!any) {
             if (aborted(p)) break;
             const long u = atomicAdd(p.w.ctl + 0, 1);
             if (!unit_of(p, u, max_steps, rec)) break;
             any = rec[U_VALID] != 0;
         }
         if (!any) rec[U_VALID] = 0;
+    };
+    grab(P.pu);
+    for (uint32_t h = 0; ok; ++h) {
+        int *rec = P.pu + 16 * (h & 1);
+        const bool any = rec[U_VALID] != 0;
         mbar_arrive(B + PB_UREADY);
         if (!any) break;
         // the raw buffer is free once the previous unit's last reader (the Z epilogue) is done,
@@ -775,6 +780,9 @@ __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
             tma_load_3d(P.sm + PP_RAW + kb * 16384, tm_k, kb * 64, rec[U_HK], rec[U_TOK], B + PB_TMA);
             tma_load_3d(P.sm + PP_RAW + kb * 16384 + 8192, tm_q, kb * 64, rec[U_HK], rec[U_TOK], B + PB_TMA);
         }
+        // the next unit, found while this one is prepared (the math threads read the other record
+        // at the start of the unit before this one, which ended before RAWFREE above)
+        grab(P.pu + 16 * ((h + 1) & 1));
         tma_pending = 1 + (int)(h & 1);
         if (!wait_bar(B + PB_TMA, h & 1, kDrainBudget)) { ok = false; break; }
         tma_pending = 0;
@@ -875,8 +883,9 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
     for (uint32_t h = 0;; ++h) {
         bool ab = !wait_bar(B + PB_UREADY, h & 1, budget);
         if (bar_any(bar_id, 128, ab)) { failed = true; break; }
-        if (P.pu[U_VALID] == 0) break;
-        const int us = P.pu[U_S], ri = P.pu[U_RI], hv = P.pu[U_H], tok0 = P.pu[U_TOK], L = P.pu[U_L];
+        const int *ur = P.pu + 16 * (h & 1);
+        if (ur[U_VALID] == 0) break;
+        const int us = ur[U_S], ri = ur[U_RI], hv = ur[U_H], tok0 = ur[U_TOK], L = ur[U_L];
         // ---- gates: loads issued now, used once the tiles and the Gram are ready (their latency hides) ----
         // (raw 16-bit values: converting them here would wait for the loads)
         unsigned short g0 = 0, g1 = 0, bl = 0;

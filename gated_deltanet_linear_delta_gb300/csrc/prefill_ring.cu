@@ -196,11 +196,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t par, long long 
 }
 
 // T = (I + A)^-1, A strictly lower 64 x 64 fp32 with row stride LS; 128 threads of named barrier
-// `bar_id`. The diagonal 16 x 16 blocks by forward substitution (one column per thread, loads issued
-// two steps ahead); then block levels d = 1..3, T_ij = -T_ii (sum_{k=j}^{i-1} A_ik T_kj) with
-// i = j + d, four threads per output column (thread q holds rows q, q+4, q+8, q+12): the column of
-// the inner sum is exchanged by shuffles inside the quad, so each level is one phase. Every stage
-// issues its shared-memory loads before its FMAs.
+// `bar_id`, in four barrier-separated phases: (1) the four diagonal 16x16 blocks by forward
+// substitution (one column per thread, loads issued two steps ahead); (2) inside each 32x32
+// diagonal block, T10 = -T11 (A10 T00) (64 threads per block, four per output column: thread q
+// holds rows q, q+4, q+8, q+12, and the column of the inner product is exchanged by shuffles in
+// the quad); (3) the 32x32 lower-left block, X = A_HL T_LL and then T_HL = -T_HH X, 2 x 4 outputs
+// per thread with X passed through the (zero) upper-right block. Block-triangular zeros are
+// skipped; every stage issues its shared-memory loads before its FMAs.
 __device__ void solve128(const float *sA, float *sT, int p, int bar_id) {
     if (p < 64) {
         const int b = p >> 4, c = p & 15;
@@ -225,6 +227,7 @@ __device__ void solve128(const float *sA, float *sT, int p, int bar_id) {
         float *Tb = sT + 16 * b * LS + 16 * b + c;
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tb[r * LS] = x[r];
+        // zeros above the diagonal blocks (the 32-block zeros are written in step 3's layout too)
 #pragma unroll
         for (int i = 0; i < 3; ++i)
             if (i < b)
@@ -232,74 +235,118 @@ __device__ void solve128(const float *sA, float *sT, int p, int bar_id) {
                 for (int r = 0; r < 16; ++r) sT[(16 * i + r) * LS + 16 * b + c] = 0.f;
     }
     bar_sync(bar_id, 128);
-    const int lane = p & 31, q = p & 3, col = (p >> 2) & 15;
-#pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-#pragma unroll 1
-        for (int blk = p >> 6; blk < 4 - d; blk += 2) {
-            const int j = blk, i = j + d;
-            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-#pragma unroll 1
-            for (int k = j; k < i; ++k) {
-                const float *Ar = sA + (16 * i + q) * LS + 16 * k;
-                const float *Tc = sT + 16 * k * LS + 16 * j + col;
-                float t[16];
-                float4 a[4][4];
+    {   // step 2: blocks (1,0) and (3,2); thread (col, q) of its 64: rows q, q+4, q+8, q+12 of column col
+        const int lane = p & 31, q = p & 3, col = (p >> 2) & 15, j = 2 * (p >> 6), i = j + 1;
+        const float *Ar = sA + (16 * i + q) * LS + 16 * j;
+        const float *Tc = sT + 16 * j * LS + 16 * j + col;
+        float t[16];
+        float4 a[4][4];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) t[m] = Tc[m * LS];
+        for (int m = 0; m < 16; ++m) t[m] = Tc[m * LS];
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr)
+        for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
-                    for (int m4 = 0; m4 < 4; ++m4) a[rr][m4] = *reinterpret_cast<const float4 *>(Ar + 4 * rr * LS + 4 * m4);
-                float acc[4][2];
+            for (int m4 = 0; m4 < 4; ++m4) a[rr][m4] = *reinterpret_cast<const float4 *>(Ar + 4 * rr * LS + 4 * m4);
+        float xs[4];
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) acc[rr][0] = acc[rr][1] = 0.f;
+        for (int rr = 0; rr < 4; ++rr) {
+            float e0 = 0.f, e1 = 0.f;
 #pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4)
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        float &e = acc[rr][m4 & 1];
-                        e = fmaf(a[rr][m4].x, t[4 * m4], e);
-                        e = fmaf(a[rr][m4].y, t[4 * m4 + 1], e);
-                        e = fmaf(a[rr][m4].z, t[4 * m4 + 2], e);
-                        e = fmaf(a[rr][m4].w, t[4 * m4 + 3], e);
-                    }
-                x0 += acc[0][0] + acc[0][1];
-                x1 += acc[1][0] + acc[1][1];
-                x2 += acc[2][0] + acc[2][1];
-                x3 += acc[3][0] + acc[3][1];
+            for (int m4 = 0; m4 < 4; ++m4) {
+                float &e = (m4 & 1) ? e1 : e0;
+                e = fmaf(a[rr][m4].x, t[4 * m4], e);
+                e = fmaf(a[rr][m4].y, t[4 * m4 + 1], e);
+                e = fmaf(a[rr][m4].z, t[4 * m4 + 2], e);
+                e = fmaf(a[rr][m4].w, t[4 * m4 + 3], e);
             }
-            const float *Tr = sT + (16 * i + q) * LS + 16 * i;
-            float4 tt[4][4];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4) tt[rr][m4] = *reinterpret_cast<const float4 *>(Tr + 4 * rr * LS + 4 * m4);
-            float X[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int src = (lane & ~3) | (m & 3);
-                const float v = (m >> 2) == 0 ? x0 : (m >> 2) == 1 ? x1 : (m >> 2) == 2 ? x2 : x3;
-                X[m] = __shfl_sync(0xffffffffu, v, src);
-            }
-            float y[4][2];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = 0.f;
-#pragma unroll
-            for (int m4 = 0; m4 < 4; ++m4)
-#pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    float &e = y[rr][m4 & 1];
-                    e = fmaf(tt[rr][m4].x, X[4 * m4], e);
-                    e = fmaf(tt[rr][m4].y, X[4 * m4 + 1], e);
-                    e = fmaf(tt[rr][m4].z, X[4 * m4 + 2], e);
-                    e = fmaf(tt[rr][m4].w, X[4 * m4 + 3], e);
-                }
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) sT[(16 * i + q + 4 * rr) * LS + 16 * j + col] = -(y[rr][0] + y[rr][1]);
+            xs[rr] = e0 + e1;
         }
-        bar_sync(bar_id, 128);
+        const float *Tr = sT + (16 * i + q) * LS + 16 * i;
+        float4 tt[4][4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int m4 = 0; m4 < 4; ++m4) tt[rr][m4] = *reinterpret_cast<const float4 *>(Tr + 4 * rr * LS + 4 * m4);
+        float X[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) X[m] = __shfl_sync(0xffffffffu, xs[m >> 2], (lane & ~3) | (m & 3));
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+            for (int m4 = 0; m4 < 4; ++m4) {
+                float &e = (m4 & 1) ? e1 : e0;
+                e = fmaf(tt[rr][m4].x, X[4 * m4], e);
+                e = fmaf(tt[rr][m4].y, X[4 * m4 + 1], e);
+                e = fmaf(tt[rr][m4].z, X[4 * m4 + 2], e);
+                e = fmaf(tt[rr][m4].w, X[4 * m4 + 3], e);
+            }
+            sT[(16 * i + q + 4 * rr) * LS + 16 * j + col] = -(e0 + e1);
+        }
     }
+    bar_sync(bar_id, 128);
+    // step 3: X = A[32:64, 0:32] T[0:32, 0:32] (T lower: X[:, n] sums k >= 16*(n/16) only), kept in
+    // registers as a 2 x 4 tile (rows 2*rg, 2*rg + 1; columns 4*cg .. 4*cg + 3); then
+    // T[32+r, n] = -sum_{k <= r} T[32+r, 32+k] X[k, n], the X rows exchanged through shared memory.
+    const int cg = p & 7, rg = p >> 3, c0 = 4 * cg, r0 = 2 * rg;
+    float acc[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
+    {
+        const int k0 = c0 & 16;  // T[k][c] = 0 for k < 16 when c >= 16
+#pragma unroll 4
+        for (int k4 = k0; k4 < 32; k4 += 4) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(sA + (32 + r0) * LS + k4);
+            const float4 a1 = *reinterpret_cast<const float4 *>(sA + (33 + r0) * LS + k4);
+            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(sT + (k4 + kk) * LS + c0);
+                acc[0][0] = fmaf(av0[kk], t4.x, acc[0][0]); acc[0][1] = fmaf(av0[kk], t4.y, acc[0][1]);
+                acc[0][2] = fmaf(av0[kk], t4.z, acc[0][2]); acc[0][3] = fmaf(av0[kk], t4.w, acc[0][3]);
+                acc[1][0] = fmaf(av1[kk], t4.x, acc[1][0]); acc[1][1] = fmaf(av1[kk], t4.y, acc[1][1]);
+                acc[1][2] = fmaf(av1[kk], t4.z, acc[1][2]); acc[1][3] = fmaf(av1[kk], t4.w, acc[1][3]);
+            }
+        }
+    }
+    // X goes to the (still zero) upper-right block T[0:32, 32:64] as scratch: row r of X at T[r][32..63]
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+        *reinterpret_cast<float4 *>(sT + (r0 + u) * LS + 32 + c0) = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+    bar_sync(bar_id, 128);
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
+    {
+        const int kend = r0 + 2;  // T[32+r][32+k] = 0 for k > r
+#pragma unroll 2
+        for (int k4 = 0; k4 < kend; k4 += 4) {
+            const float4 h0 = *reinterpret_cast<const float4 *>(sT + (32 + r0) * LS + 32 + k4);
+            const float4 h1 = *reinterpret_cast<const float4 *>(sT + (33 + r0) * LS + 32 + k4);
+            const float hv0[4] = {h0.x, h0.y, h0.z, h0.w}, hv1[4] = {h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 x4 = *reinterpret_cast<const float4 *>(sT + (k4 + kk) * LS + 32 + c0);
+                acc[0][0] = fmaf(hv0[kk], x4.x, acc[0][0]); acc[0][1] = fmaf(hv0[kk], x4.y, acc[0][1]);
+                acc[0][2] = fmaf(hv0[kk], x4.z, acc[0][2]); acc[0][3] = fmaf(hv0[kk], x4.w, acc[0][3]);
+                acc[1][0] = fmaf(hv1[kk], x4.x, acc[1][0]); acc[1][1] = fmaf(hv1[kk], x4.y, acc[1][1]);
+                acc[1][2] = fmaf(hv1[kk], x4.z, acc[1][2]); acc[1][3] = fmaf(hv1[kk], x4.w, acc[1][3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+        *reinterpret_cast<float4 *>(sT + (32 + r0 + u) * LS + c0) =
+            make_float4(-acc[u][0], -acc[u][1], -acc[u][2], -acc[u][3]);
+    bar_sync(bar_id, 128);
+    // the scratch block back to zero
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+        *reinterpret_cast<float4 *>(sT + (r0 + u) * LS + 32 + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+    bar_sync(bar_id, 128);
 }
 
 // Chain id of list position `pos` of chain CTA (group m, member v). Chains are numbered

@@ -78,6 +78,37 @@ def test_prefill_zero_batch_is_a_noop(lib):
     assert prefill(lib, B=0) == 0
 
 
+def prefill_static(lib, **kw):
+    args = dict(q=A, k=A, v=A, g=A, b=A, si=None, so=A, out=A, cu=None, B=1, T=64, Hk=2, Hv=4,
+                dk=128, dv=128, chunk=64, dtype=0)
+    args.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.gdn_prefill_static(p(args["q"]), p(args["k"]), p(args["v"]), p(args["g"]), p(args["b"]),
+                                  p(args["si"]), p(args["so"]), p(args["out"]), p(args["cu"]), args["B"],
+                                  args["T"], args["Hk"], args["Hv"], args["dk"], args["dv"], args["chunk"],
+                                  args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=48), -2), (dict(chunk=128), -2), (dict(Hk=3, Hv=4), -1), (dict(B=-1), -1),
+    (dict(q=A + 2), -1), (dict(so=None), -1),
+])
+def test_prefill_static_rejects(lib, kw, code):
+    assert prefill_static(lib, **kw) == code
+
+
+def test_prefill_static_zero_batch_is_a_noop(lib):
+    assert prefill_static(lib, B=0) == 0
+
+
+@pytest.mark.parametrize("sizes", [
+    (1, 64, 2, 4, 48, 128, 64, 0), (1, 64, 3, 4, 128, 128, 64, 0), (-1, 64, 2, 4, 128, 128, 64, 0),
+    (0, 64, 2, 4, 128, 128, 64, 0), (1, 64, 2, 4, 128, 128, 128, 0),
+])
+def test_workspace_size_is_zero_for_rejected_or_empty_sizes(lib, sizes):
+    assert lib.gdn_prefill_workspace_size(*sizes) == 0
+
+
 def decode(lib, **kw):
     args = dict(q=A, k=A, v=A, g=A, b=A, st=A, out=A, N=4, Hk=2, Hv=4, dk=128, dv=128, dtype=0)
     args.update(kw)

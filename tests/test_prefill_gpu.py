@@ -62,6 +62,17 @@ def test_shapes_ragged(dtype, dk, dv, chunk):
     check(b, out, so)
 
 
+@pytest.mark.parametrize("hk,hv", [(3, 3), (2, 8), (1, 8), (5, 10), (40, 80)])
+def test_head_groups_on_the_tensor_core_kernel(hk, hv):
+    """Value heads per key head r = 1, 4, 8, 2 (odd key-head count) and more chains than state
+    CTAs (80 heads x 3 sequences): the state CTAs are dealt in groups of r, several chains each."""
+    b = inputs.make_batch(Hk=hk, Hv=hv, dk=128, dv=128, dtype="bf16", chunk=64, seed=hk * 100 + hv,
+                          init_state=True, lengths=[190, 64, 333] if hv < 80 else [65, 1, 130])
+    assert gdn.gdn_prefill_path(3, 600, hk, hv, 128, 128, 64, gdn.GDN_BF16) == 1
+    out, so = run_prefill(b)
+    check(b, out, so, key_heads=None if hk <= 5 else [0, 17, 39])
+
+
 @pytest.mark.parametrize("lengths", [[0, 1, 63, 64, 65, 130, 7], [200], [1], [64, 64, 64]])
 def test_varlen_edges_qwen_heads(lengths):
     """Packed sequences with empty, single-token and partial-last-block members."""

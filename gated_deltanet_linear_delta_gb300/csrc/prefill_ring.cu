@@ -25,9 +25,10 @@
 //    tcgen05 MMAs (S N and S Z with an fp16 copy of S in TMEM; V^T B and V^T E on the raw bf16
 //    V tile with B, E as bf16 hi + lo pairs, B sent as B^T rows), the state update and the bf16
 //    outputs;
-//  * prep CTAs: take (key head, block) units from a global counter, compute norms, gates, A,
-//    P, the triangular solve and N, Z, B, E for every value head of the key head, and write
-//    them into a per-chain ring of slots in device memory that the chain CTA bulk-copies in.
+//  * prep CTAs: take (block, value head) units from a global counter, compute norms, gates, A,
+//    P, the triangular solve and N, Z, B, E, and write them into a per-chain ring of slots in
+//    device memory that the chain CTA bulk-copies in. With more chains than chain CTAs a
+//    pipeline takes the value heads of one key head in a row and does the key-side work once.
 // Ring protocol: slot k of chain CTA i holds its step s = k (mod slots) once
 // slot_seq[i][k] == s + 1 (release/acquire at GPU scope); the chain publishes consumed[i] =
 // s + 1 when step s's copy has landed, and a prep CTA writes step s only once step s - slots
@@ -44,6 +45,7 @@
 // word and a launch-wide abort flag, and every role leaves after draining its own asynchronous
 // copies and MMAs.
 #include <cuda.h>
+#include <type_traits>
 #include <cstdio>
 #include <cstdlib>
 #include <cuda_fp16.h>
@@ -119,12 +121,14 @@ constexpr int PS_BBRK = 448;   // e^{gmin - G_s} rk_s
 constexpr int PS_TWF = 512;    // beta_s e_s rk_s           (Tw' columns)
 constexpr int PS_DRK = 576;    // d_s rk_s                  (Tb' rows, W^T d columns)
 constexpr int PS_ER = 640;     // e_t rq_t                   (Qt rows)
-constexpr int PS_MISC = 704;   // gmin, gmax, factor flag, gamma, 1 / sigma
+constexpr int PS_MISC = 704;   // gmin, gmax, factor flag, gamma, 1 / sigma, 1 / sigma_q
 constexpr int PS_RED = 720;    // [4 warps] reductions
-constexpr int PS_UNIT = 768;   // int[2][16]: unit records, unit h in [h & 1]
+constexpr int PS_UNIT = 768;   // int[3][16]: unit records, unit h in [h & 1]; [2]: the next group's first
 constexpr int PS_MAIL = 752;   // int[4]: to the publisher: [0] ring CTA (-1: stop), [1] step, [2] gamma bits, [3] failed
 // unit record (int offsets)
-constexpr int U_VALID = 0, U_S = 1, U_RI = 2, U_H = 3, U_HK = 4, U_TOK = 5, U_L = 6;
+// U_VI: the unit's place among the r value heads of its key head when one pipeline prepares all r
+// in a row and shares the key-side work; U_LAST: the group's last unit
+constexpr int U_VALID = 0, U_S = 1, U_RI = 2, U_H = 3, U_HK = 4, U_TOK = 5, U_L = 6, U_VI = 7, U_LAST = 8;
 // pipeline mbarriers (index into PP_BAR)
 constexpr int PB_UREADY = 0, PB_TMA = 1, PB_G = 2, PB_M1REQ = 3, PB_M1 = 4, PB_M2REQ = 5, PB_M2 = 6, PB_RAWFREE = 7,
               PB_BEREADY = 8, PB_BEREAD = 9, PB_NZREADY = 10, PB_STGFREE = 11, PB_FIN = 12, PB_COUNT = 13;
@@ -140,6 +144,7 @@ constexpr uint32_t ID_VE = idesc_bf16(128, 64, 1, 1);   // V^T x E (hi or lo)
 constexpr uint32_t ID_SN = idesc_f16(128, 128, 0, 1);   // S16 (TMEM) x N
 constexpr uint32_t ID_SZ = idesc_f16(128, 64, 0, 1);    // S16 (TMEM) x Z
 constexpr uint32_t ID_GRAM = idesc_bf16(128, 64, 0, 0); // [K; Q] K^T on raw tiles
+constexpr uint32_t ID_GRAM16 = idesc_f16(128, 64, 0, 0); // [K'; Q'] K'^T on the converted tiles
 constexpr uint32_t ID_WT = idesc_f16(128, 64, 1, 0);    // K'^T Tw'^T (K' = sigma K in fp16)
 constexpr uint32_t ID_B = idesc_f16(128, 64, 1, 1);     // K'^T Tb' = sigma B^T (Tb' hi or lo, fp16)
 constexpr uint32_t ID_E = idesc_f16(64, 64, 1, 0);      // Tb^T P^T
@@ -793,6 +798,7 @@ __device__ bool unit_of(const RingParams &p, long u, int max_steps, int *rec) {
 }
 
 // ---- control thread: units, tile loads, every MMA ----
+template <bool SHARE>
 __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, const RingParams &p, const Pipe &P) {
     const long long budget = p.wait_budget;
     const int max_steps = p.w.ctl[64];
@@ -801,43 +807,67 @@ __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
     int tma_pending = 0;
     prefetch_tmap(tm_q);
     prefetch_tmap(tm_k);
-    // next unit with work into rec (rec[U_VALID] = 0: none left)
+    // The first unit of the next group with work into rec (rec[U_VALID] = 0: none left). With SHARE,
+    // units come from the counter r at a time: the r value heads of one key head at one step,
+    // prepared in a row with the key-side work done once (fewer instructions per unit, one more unit
+    // latency before a step's last value head: taken when there are more chains than state CTAs,
+    // i.e. when throughput matters more than latency). Without it a group is one unit.
     auto grab = [&](int *rec) {
         bool any = false;
         while (!any) {
             if (aborted(p)) break;
-            const long u = atomicAdd(p.w.ctl + 0, 1);
+            const long u = atomicAdd(p.w.ctl + 0, SHARE ? p.r : 1);
             if (!unit_of(p, u, max_steps, rec)) break;
             any = rec[U_VALID] != 0;
         }
         if (!any) rec[U_VALID] = 0;
+        if constexpr (SHARE) {
+            rec[U_VI] = 0;
+            rec[U_LAST] = 0;
+        }
     };
+    int *const gnext = P.pu + 32;  // the next group's first unit (SHARE)
     grab(P.pu);
+    uint32_t g = 0;  // groups started
     for (uint32_t h = 0; ok; ++h) {
         int *rec = P.pu + 16 * (h & 1);
         const bool any = rec[U_VALID] != 0;
+        const int vi = SHARE ? rec[U_VI] : 0;
         mbar_arrive(B + PB_UREADY);
         if (!any) break;
-        // the raw buffer is free once the previous unit's last reader (the Z epilogue) is done,
-        // which is after its second MMA batch: the Gram below may also overwrite its TMEM operands
-        if (h > 0 && !wait_bar(B + PB_RAWFREE, (h - 1) & 1, budget)) { ok = false; break; }
-        mbar_expect_tx(B + PB_TMA, 4 * 8192);
+        if (vi == 0) {
+            // the raw buffer is free once the previous group's last reader (its last Z epilogue) is
+            // done, which is after its last second MMA batch: the Gram below overwrites its TMEM operands
+            if (g > 0 && !wait_bar(B + PB_RAWFREE, (g - 1) & 1, budget)) { ok = false; break; }
+            mbar_expect_tx(B + PB_TMA, 4 * 8192);
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_3d(P.sm + PP_RAW + kb * 16384, tm_k, kb * 64, rec[U_HK], rec[U_TOK], B + PB_TMA);
-            tma_load_3d(P.sm + PP_RAW + kb * 16384 + 8192, tm_q, kb * 64, rec[U_HK], rec[U_TOK], B + PB_TMA);
-        }
-        // the next unit, found while this one is prepared (the math threads read the other record
-        // at the start of the unit before this one, which ended before RAWFREE above)
-        grab(P.pu + 16 * ((h + 1) & 1));
-        tma_pending = 1 + (int)(h & 1);
-        if (!wait_bar(B + PB_TMA, h & 1, kDrainBudget)) { ok = false; break; }
-        tma_pending = 0;
-        tc_fence_after();
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_3d(P.sm + PP_RAW + kb * 16384, tm_k, kb * 64, rec[U_HK], rec[U_TOK], B + PB_TMA);
+                tma_load_3d(P.sm + PP_RAW + kb * 16384 + 8192, tm_q, kb * 64, rec[U_HK], rec[U_TOK], B + PB_TMA);
+            }
+            // the next group, found while this one is prepared (without SHARE straight into the other
+            // record: the math threads read it at the start of the unit before this one, which ended
+            // before RAWFREE above)
+            grab(SHARE ? gnext : P.pu + 16 * ((h + 1) & 1));
+            tma_pending = 1 + (int)(g & 1);
+            if (!wait_bar(B + PB_TMA, g & 1, kDrainBudget)) { ok = false; break; }
+            tma_pending = 0;
+            tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // Gram [K; Q] K^T on the raw bf16 tiles (exact products)
-            const uint64_t d = desc_sw128(P.sb + PP_RAW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-            mma_bf16(P.tm + PT_G, d, d, ID_GRAM, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) {  // Gram [K; Q] K^T on the raw bf16 tiles (exact products)
+                const uint64_t d = desc_sw128(P.sb + PP_RAW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                mma_bf16(P.tm + PT_G, d, d, ID_GRAM, ks > 0);
+            }
+        } else {
+            // the same tiles, now K' and Q' in fp16: the Gram again (times sigma^2 on the K rows,
+            // sigma sigma_q on the Q rows), once the previous unit's second batch has left TMEM
+            if (!wait_bar(B + PB_M2, (h - 1) & 1, kDrainBudget)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t d = desc_sw128(P.sb + PP_RAW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                mma_f16_ss(P.tm + PT_G, d, d, ID_GRAM16, ks > 0);
+            }
         }
         mma_commit(B + PB_G);
         if (!wait_bar(B + PB_M1REQ, h & 1, budget)) { ok = false; break; }
@@ -868,6 +898,23 @@ __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
             mma_f16_ts(P.tm + PT_WP, P.tm + PT_WT + 32 + 8 * ks, desc_sw128(P.sb + PP_P + ks * 32, 16, 1024), ID_WP,
                        ks > 0);
         mma_commit(B + PB_M2);
+        if constexpr (SHARE) {  // the next unit's record: this group's next value head, or the next group's first
+            int *nrec = P.pu + 16 * ((h + 1) & 1);
+            if (vi + 1 < p.r) {
+#pragma unroll
+                for (int f = 0; f < 16; ++f) nrec[f] = rec[f];
+                nrec[U_RI] = rec[U_RI] + 1;
+                nrec[U_H] = rec[U_H] + 1;
+                nrec[U_VI] = vi + 1;
+                nrec[U_LAST] = vi + 2 == p.r;
+            } else {
+#pragma unroll
+                for (int f = 0; f < 16; ++f) nrec[f] = gnext[f];
+                ++g;
+            }
+        } else {
+            ++g;
+        }
     }
     if (tma_pending) wait_bar(B + PB_TMA, (uint32_t)(tma_pending - 1), kDrainBudget);  // tiles still landing
     mma_commit(B + PB_FIN);
@@ -917,6 +964,7 @@ __device__ void prep_publisher(const RingParams &p, const Pipe &P) {
 }
 
 // ---- math threads (128) ----
+template <bool SHARE>
 __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id) {
     const int warp = mt >> 5, lane = mt & 31;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -933,6 +981,8 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         const int *ur = P.pu + 16 * (h & 1);
         if (ur[U_VALID] == 0) break;
         const int us = ur[U_S], ri = ur[U_RI], hv = ur[U_H], tok0 = ur[U_TOK], L = ur[U_L];
+        const int vi = SHARE ? ur[U_VI] : 0;  // > 0: the key-side work of this key head is done
+        const bool last_of_group = SHARE ? ur[U_LAST] != 0 : true;
         // ---- gates: loads issued now, used once the tiles and the Gram are ready (their latency hides) ----
         // (raw 16-bit values: converting them here would wait for the loads)
         unsigned short g0 = 0, g1 = 0, bl = 0;
@@ -986,7 +1036,7 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
                 ps[PS_MISC + 3] = expf(GL);
             }
         }
-        {  // row norms of [K; Q] (row mt) and the K tile's largest magnitude
+        if (vi == 0) {  // row norms of [K; Q] (row mt) and the largest magnitude of the K (and Q) tile
             float ssq = 0.f, kmax = 0.f;
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb)
@@ -1003,25 +1053,36 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
             const int row = mt & 63;
             const float rn = row < L ? rsqrtf(ssq + kNormEps) : 0.f;
             (mt < 64 ? ps + PS_RK : ps + PS_RQ)[row] = rn;
-            kmax = warp_max(mt < 64 && row < L ? kmax : 0.f);
+            kmax = warp_max((SHARE || mt < 64) && row < L ? kmax : 0.f);
             if (lane == 0) ps[PS_RED + warp] = kmax;
         }
-        bar_sync(bar_id, 128);
-        {
-            const float km = fmaxf(ps[PS_RED + 0], ps[PS_RED + 1]);  // K rows are warps 0, 1
-            // K' = sigma K stays below 2^14 in fp16; every product with K' is taken back by 1 / sigma
-            // in fp32 in its epilogue (the fp16 operands keep their natural range)
-            const float sigma = pow2_scale(km);
-            if (mt < 64) {
-                const float rk = ps[PS_RK + mt];
-                ps[PS_BBRK + mt] = expf(ps[PS_MISC + 0] - ps[PS_G + mt]) * rk;
-                ps[PS_TWF + mt] = ps[PS_BETA + mt] * ps[PS_E + mt] * rk;
-                ps[PS_DRK + mt] = ps[PS_D + mt] * rk;
-                ps[PS_ER + mt] = ps[PS_E + mt] * ps[PS_RQ + mt];
-                if (mt == 0) ps[PS_MISC + 4] = 1.f / sigma;
+        float iq = 1.f, sigma = 1.f, sigma_q = 1.f;  // iq = 1 / sigma_q when the Z epilogue reads Q'
+        if (vi == 0) {
+            bar_sync(bar_id, 128);
+            // K' = sigma K (and, with SHARE, Q' = sigma_q Q) stay below 2^14 in fp16; every product
+            // with them is taken back in fp32 in its epilogue (the fp16 operands keep their natural range)
+            sigma = pow2_scale(fmaxf(ps[PS_RED + 0], ps[PS_RED + 1]));  // K rows: warps 0, 1
+            if constexpr (SHARE) {
+                sigma_q = pow2_scale(fmaxf(ps[PS_RED + 2], ps[PS_RED + 3]));
+                iq = 1.f / sigma_q;
             }
-            // K rows -> K' = sigma K in fp16, in place (the Gram that read them is complete); rows
-            // beyond L (the next sequence, or past the end) become zero
+        } else {
+            iq = ps[PS_MISC + 5];
+        }
+        if (mt < 64) {  // the gate-dependent row scalars (rk, rq and the scales are the key head's)
+            const float rk = ps[PS_RK + mt];
+            ps[PS_BBRK + mt] = expf(ps[PS_MISC + 0] - ps[PS_G + mt]) * rk;
+            ps[PS_TWF + mt] = ps[PS_BETA + mt] * ps[PS_E + mt] * rk;
+            ps[PS_DRK + mt] = ps[PS_D + mt] * rk;
+            ps[PS_ER + mt] = SHARE ? ps[PS_E + mt] * ps[PS_RQ + mt] * iq : ps[PS_E + mt] * ps[PS_RQ + mt];  // Qt rows
+            if (mt == 0 && vi == 0) {
+                ps[PS_MISC + 4] = 1.f / sigma;
+                if constexpr (SHARE) ps[PS_MISC + 5] = iq;
+            }
+        }
+        if (vi == 0) {
+            // K (and with SHARE Q) rows -> fp16, in place (the Gram that read them is complete); rows
+            // beyond L (the next sequence, or past the end) become zero. A group's later units use them.
             const int t = mt & 63, kb = mt >> 6;
             const float sg = t < L ? sigma : 0.f;
 #pragma unroll
@@ -1031,6 +1092,16 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
                 unpack8(*pk, x);
                 *pk = pack8_f16(x, sg);
             }
+            if constexpr (SHARE) {
+                const float sq = t < L ? sigma_q : 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 *pq = reinterpret_cast<uint4 *>(sm + PP_RAW + kb * 16384 + swz(64 + t, c));
+                    float y[8];
+                    unpack8(*pq, y);
+                    *pq = pack8_f16(y, sq);
+                }
+            }
         }
         fence_async_smem();
         // the previous unit's staged images must be read out before A, T and the tiles overwrite them
@@ -1039,7 +1110,11 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         {  // A rows (fp32) and P rows (fp16) from the Gram: thread mt reads Gram row mt
             const int row = mt & 63;
             const bool isq = mt >= 64;
-            const float nt = isq ? ps[PS_RQ + row] : ps[PS_RK + row] * ps[PS_BETA + row];
+            float nt = isq ? ps[PS_RQ + row] : ps[PS_RK + row] * ps[PS_BETA + row];
+            if (SHARE && vi > 0) {  // a group's later units: the fp16 Gram carries sigma^2 (K rows), sigma sigma_q (Q rows)
+                const float isg = ps[PS_MISC + 4];
+                nt *= isq ? isg * iq : isg * isg;
+            }
             uint32_t gv[2][32];
             tmem_ld32_nw(P.tm + lane_off + PT_G, gv[0]);
             tmem_ld32_nw(P.tm + lane_off + PT_G + 32, gv[1]);
@@ -1190,7 +1265,9 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         ab = !wait_bar(B + PB_M2, h & 1, budget);
         if (bar_any(bar_id, 128, ab)) { failed = true; break; }
         tc_fence_after();
-        {  // Z row j: Z[j][t] = e_t rq_t Q[t][j] - (W^T P^T)[j][t] -> fp16 image (MN-major [j][t]) in TT
+        // Z row j: Z[j][t] = e_t rq_t Q[t][j] - (W^T P^T)[j][t] -> fp16 image (MN-major [j][t]) in TT,
+        // Q read raw (bf16) or, with SHARE, as Q' (fp16; ER carries 1 / sigma_q)
+        auto z_epilogue = [&](auto q_is_f16) {
             const int j = mt, qb = j >> 6, qc = (j & 63) >> 3, qe = j & 7;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -1203,16 +1280,21 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int t = 32 * q + 8 * cc + e, row = 64 + t;
-                        const __nv_bfloat16 qv = *reinterpret_cast<const __nv_bfloat16 *>(
-                            sm + PP_RAW + qb * 16384 + row * 128 + ((qc ^ (row & 7)) << 4) + 2 * qe);
-                        x[e] = ps[PS_ER + t] * __bfloat162float(qv) - __uint_as_float(wv[8 * cc + e]);
+                        const uint8_t *qa = sm + PP_RAW + qb * 16384 + row * 128 + ((qc ^ (row & 7)) << 4) + 2 * qe;
+                        float qf;
+                        if constexpr (decltype(q_is_f16)::value)
+                            qf = __half2float(*reinterpret_cast<const __half *>(qa));
+                        else
+                            qf = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa));
+                        x[e] = ps[PS_ER + t] * qf - __uint_as_float(wv[8 * cc + e]);
                     }
                     *reinterpret_cast<uint4 *>(sm + PP_TT + Z_STAGE + swz(j, 4 * q + cc)) = pack8_f16(x, 1.f);
                 }
             }
-        }
+        };
+        z_epilogue(std::integral_constant<bool, SHARE>{});
         bar_sync(bar_id, 128);
-        if (mt == 0) mbar_arrive(B + PB_RAWFREE);  // the raw tiles' last reader is done
+        if (mt == 0 && last_of_group) mbar_arrive(B + PB_RAWFREE);  // the tiles' last reader is done
         ab = !wait_bar(B + PB_BEREAD, h & 1, budget);  // AT holds the [B|E] head until it is read out
         if (bar_any(bar_id, 128, ab)) { failed = true; break; }
         {  // N row j -> fp16 (-N), MN-major [j][n] image in AT
@@ -1250,19 +1332,22 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
     if (failed && mt == 0) set_abort(p);
 }
 
+template <bool SHARE>
 __device__ void prep_cta(const CUtensorMap *tm_q, const CUtensorMap *tm_k, const RingParams &p, uint8_t *sm,
                          uint32_t sb, uint32_t tmem) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp < 8) {
         const int pipe = warp >> 2;
-        prep_math(p, make_pipe(sm, sb, tmem, pipe), tid & 127, 1 + pipe);
+        prep_math<SHARE>(p, make_pipe(sm, sb, tmem, pipe), tid & 127, 1 + pipe);
     } else if (lane == 0 && warp < 10) {
-        prep_control(tm_q, tm_k, p, make_pipe(sm, sb, tmem, warp - 8));
+        prep_control<SHARE>(tm_q, tm_k, p, make_pipe(sm, sb, tmem, warp - 8));
     } else if (lane == 0) {
         prep_publisher(p, make_pipe(sm, sb, tmem, warp - 10));
     }
 }
 
+// SHARE: a preparing pipeline takes the r value heads of a key head at a step in a row (see prep_control)
+template <bool SHARE>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_ring_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -1307,7 +1392,7 @@ prefill_ring_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (chain)
         chain_cta(&tm_v, &tm_o, p, sm, sb, tmem);
     else
-        prep_cta(&tm_q, &tm_k, p, sm, sb, tmem);
+        prep_cta<SHARE>(&tm_q, &tm_k, p, sm, sb, tmem);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1417,8 +1502,10 @@ cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes,
     if (!make_map(&mq, a.q, DK, a.Hk, Ttot) || !make_map(&mk, a.k, DK, a.Hk, Ttot) ||
         !make_map(&mv, a.v, DV, a.Hv, Ttot) || !make_map(&mo, a.out, DV, a.Hv, Ttot))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    // key-side sharing pays when there are more chains than state CTAs (throughput-bound)
+    const bool share = a.Hv > a.Hk && (long)a.B * a.Hv > sh.NC;
+    auto kernel = share ? prefill_ring_kernel<true> : prefill_ring_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     uint8_t *w = static_cast<uint8_t *>(ws);
     RingParams p{};
@@ -1465,7 +1552,7 @@ cudaError_t launch_prefill_ring(const PrefillArgs &a, void *ws, size_t ws_bytes,
     cfg.stream = s;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_ring_kernel, mq, mk, mv, mo, p);
+    return cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, p);
 }
 
 }  // namespace gdn

@@ -1442,11 +1442,12 @@ bool ring_shape(const PrefillArgs &a, RingShape *sh, int max_chain_ctas) {
     if (cudaDeviceGetAttribute(&sh->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     const int r = a.Hv / a.Hk;
     const long chains = (long)a.B * a.Hv;
-    // A quarter of the SMs carry states; the rest prepare blocks (measured on 16 packed sequences:
-    // 25% beats 20% and 30-40%; a single sequence needs one CTA per head, which 25% covers for 32
-    // heads). A multiple of r, so that the value heads of one key head sit in consecutive chain
-    // CTAs at the same steps.
-    long nc = std::min<long>(chains, std::max(1, sh->sms / 4));
+    // 9/38 of the SMs (36 of 152) carry states; the rest prepare blocks (measured on 16 packed
+    // sequences with key sharing: 36 state CTAs beat 32, 34, 38, 40 and 44 by 1-7%; 30 and 50 are
+    // 10-20% slower; a single sequence needs one CTA per head, which 36 covers for 32 heads). A
+    // multiple of r, so that the value heads of one key head sit in consecutive chain CTAs at the
+    // same steps.
+    long nc = std::min<long>(chains, std::max(1, sh->sms * 9 / 38));
     if (max_chain_ctas > 0) nc = std::min<long>(nc, max_chain_ctas);
     nc = std::max<long>(r, nc / r * r);
     if (nc + 8 > sh->sms) return false;

@@ -18,7 +18,10 @@ order q, k, v, g, b, state; every draw is fp32, then cast to the I/O dtype):
 
 The "slow gate" variant (g = -softplus(N(0,1)) * 1e-3, b ~ N(-2, 1)) keeps the
 state alive over thousands of tokens so that the state carried across chunks
-and calls has a visible effect on the outputs.
+and calls has a visible effect on the outputs. ``gate_scale`` multiplies the
+drawn g (after the slow-gate factor, if any): values above 1 give fast decays,
+whose in-block cumulative log-decay spans a wider range (about 51 * gate_scale
+over 64 tokens on average).
 
 Shapes (tokens packed): q, k [Ttot, Hk, dk]; v [Ttot, Hv, dv];
 g, b [Ttot, Hv]; state [B, Hv, dv, dk] (fp32); cu_seqlens int32 [B+1].
@@ -76,7 +79,8 @@ def _draws(gen, Ttot, Hk, Hv, dk, dv, slow_gate: bool):
 
 
 def make_batch(B=1, T=64, Hk=2, Hv=2, dk=32, dv=32, dtype="f32", chunk=16, seed=0,
-               init_state=False, state_std=0.02, lengths=None, slow_gate=False) -> GDNBatch:
+               init_state=False, state_std=0.02, lengths=None, slow_gate=False,
+               gate_scale=1.0) -> GDNBatch:
     """Draw one batch. ``lengths`` (a list of ints) packs variable-length sequences."""
     gen = torch.Generator().manual_seed(seed)
     if lengths is not None:
@@ -89,13 +93,15 @@ def make_batch(B=1, T=64, Hk=2, Hv=2, dk=32, dv=32, dtype="f32", chunk=16, seed=
         cu = None
         Ttot = B * T
     q, k, v, g, b = _draws(gen, Ttot, Hk, Hv, dk, dv, slow_gate)
+    if gate_scale != 1.0:
+        g = g * gate_scale
     state = None
     if init_state:
         state = torch.randn(B, Hv, dv, dk, generator=gen) * state_std
     dt = _DTYPES[dtype]
     return GDNBatch(q.to(dt), k.to(dt), v.to(dt), g.to(dt), b.to(dt), state, cu, B,
                     Ttot if cu is not None else T, Hk, Hv, dk, dv, chunk,
-                    {"seed": seed, "dtype": dtype, "slow_gate": slow_gate})
+                    {"seed": seed, "dtype": dtype, "slow_gate": slow_gate, "gate_scale": gate_scale})
 
 
 def varlen_lengths(n=16, lo=256, hi=16384, seed=0) -> list[int]:

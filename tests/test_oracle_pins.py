@@ -184,6 +184,18 @@ def test_chunked_equals_sequential(chunk):
     assert np.linalg.norm(s1 - s2) <= 1e-10 * np.linalg.norm(s1)
 
 
+@pytest.mark.parametrize("scale", [1.6, 4.0])
+def test_chunked_equals_sequential_fast_gates(scale):
+    """Decays fast enough that a 64-token block's cumulative log-decay spans ~80 to ~200: the
+    block evaluation still matches the token scan (products of e^{G_t - G_s} down to e^-200)."""
+    q, k, v, g, b, s0 = _rand(9, T=200, Hk=2, Hv=4, dk=8, dv=6, B=2)
+    g = g * scale
+    o1, s1 = oracle.gdn_sequential(q, k, v, g, b, s0, B=2)
+    o2, s2 = oracle.gdn_chunked(q, k, v, g, b, s0, B=2, chunk=64)
+    assert np.max(np.abs(o1 - o2)) <= 1e-10 * np.max(np.abs(o1))
+    assert np.linalg.norm(s1 - s2) <= 1e-10 * np.linalg.norm(s1)
+
+
 def test_chunked_equals_sequential_varlen_with_empty_and_single():
     lens = [5, 0, 1, 37, 16, 64, 3]
     T = sum(lens)

@@ -118,11 +118,11 @@ static_assert(SMEM_BYTES <= 232448, "over the 227 KiB opt-in limit");
 // prep scalars (float index into PP_SC)
 constexpr int PS_RK = 0, PS_RQ = 64, PS_G = 128, PS_BETA = 192, PS_E = 256, PS_D = 320, PS_AA = 384;
 constexpr int PS_BBRK = 448;   // e^{gmin - G_s} rk_s
-constexpr int PS_TWF = 512;    // beta_s e_s rk_s           (Tw' columns)
-constexpr int PS_DRK = 576;    // d_s rk_s                  (Tb' rows, W^T d columns)
+constexpr int PS_TWF = 512;    // beta_s e_s rk_s / kappa   (Tw' columns)
+constexpr int PS_DRK = 576;    // d_s rk_s / kappa          (Tb' rows, W^T d columns)
 constexpr int PS_ER = 640;     // e_t rq_t                   (Qt rows)
-constexpr int PS_MISC = 704;   // gmin, gmax, factor flag, gamma, 1 / sigma, 1 / sigma_q
-constexpr int PS_RED = 720;    // [4 warps] reductions
+constexpr int PS_MISC = 704;   // gmin, gmax, factor flag, gamma, 1 / sigma, 1 / sigma_q, kappa
+constexpr int PS_RED = 720;    // [4 warps] tile maxima, [4 warps] rk maxima
 constexpr int PS_UNIT = 768;   // int[3][16]: unit records, unit h in [h & 1]; [2]: the next group's first
 constexpr int PS_MAIL = 752;   // int[4]: to the publisher: [0] ring CTA (-1: stop), [1] step, [2] gamma bits, [3] failed
 // unit record (int offsets)
@@ -187,6 +187,14 @@ __device__ __forceinline__ int row_exp(float m) {
     int e;
     frexpf(m, &e);
     return max(-100, min(100, e));
+}
+
+// the power of two 2^e just above m (m < 2^e), clamped; 1 for m <= 0 or non-finite
+__device__ __forceinline__ float pow2_above(float m) {
+    if (!(m > 0.f) || !isfinite(m)) return 1.f;
+    int e;
+    frexpf(m, &e);
+    return ldexpf(1.f, max(-100, min(100, e)));
 }
 
 __device__ __forceinline__ void set_abort(const RingParams &p) {
@@ -873,11 +881,11 @@ __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
         if (!wait_bar(B + PB_M1REQ, h & 1, budget)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks)  // W^T = K'^T Tw'^T
+        for (int ks = 0; ks < 4; ++ks)  // (sigma / kappa) W^T = K'^T Tw'^T
             mma_f16_ss(P.tm + PT_WT, desc_sw128(P.sb + PP_RAW + ks * 2048, 16384, 1024),
                        desc_sw128(P.sb + PP_TT + ks * 32, 16, 1024), ID_WT, ks > 0);
 #pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks) {  // sigma B^T = K'^T Tb' (hi + lo)
+        for (int ks = 0; ks < 4; ++ks) {  // (sigma / kappa) B^T = K'^T Tb' (hi + lo)
             const uint64_t ak = desc_sw128(P.sb + PP_RAW + ks * 2048, 16384, 1024);
             mma_f16_ss(P.tm + PT_B, ak, desc_sw128(P.sb + PP_TT + 16384 + ks * 2048, 8192, 1024), ID_B, ks > 0);
             mma_f16_ss(P.tm + PT_B, ak, desc_sw128(P.sb + PP_TT + 24576 + ks * 2048, 8192, 1024), ID_B, 1);
@@ -890,7 +898,7 @@ __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
         if (!wait_bar(B + PB_M2REQ, h & 1, budget)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks)  // sigma N = (W^T diag(d rk)) K', A = WTd' from TMEM
+        for (int ks = 0; ks < 4; ++ks)  // (sigma / kappa) N = -(W^T diag(d rk / kappa)) K', A = WTd' from TMEM
             mma_f16_ts(P.tm + PT_N, P.tm + PT_WT + 8 * ks, desc_sw128(P.sb + PP_RAW + ks * 2048, 16384, 1024), ID_N,
                        ks > 0);
 #pragma unroll 1
@@ -1054,29 +1062,39 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
             const float rn = row < L ? rsqrtf(ssq + kNormEps) : 0.f;
             (mt < 64 ? ps + PS_RK : ps + PS_RQ)[row] = rn;
             kmax = warp_max((SHARE || mt < 64) && row < L ? kmax : 0.f);
-            if (lane == 0) ps[PS_RED + warp] = kmax;
+            const float rkmax = warp_max(mt < 64 ? rn : 0.f);
+            if (lane == 0) {
+                ps[PS_RED + warp] = kmax;
+                ps[PS_RED + 4 + warp] = rkmax;
+            }
         }
-        float iq = 1.f, sigma = 1.f, sigma_q = 1.f;  // iq = 1 / sigma_q when the Z epilogue reads Q'
+        // iq = 1 / sigma_q when the Z epilogue reads Q'; kappa: a power of two at or above every rk
+        float iq = 1.f, sigma = 1.f, sigma_q = 1.f, kappa;
         if (vi == 0) {
             bar_sync(bar_id, 128);
             // K' = sigma K (and, with SHARE, Q' = sigma_q Q) stay below 2^14 in fp16; every product
             // with them is taken back in fp32 in its epilogue (the fp16 operands keep their natural range)
             sigma = pow2_scale(fmaxf(ps[PS_RED + 0], ps[PS_RED + 1]));  // K rows: warps 0, 1
+            // rk enters the fp16 operands Tw', Tb' and W^T diag(d rk) as rk / kappa (at most 1): for
+            // keys of large norm rk itself would put them among fp16's subnormals
+            kappa = pow2_above(fmaxf(ps[PS_RED + 4], ps[PS_RED + 5]));
             if constexpr (SHARE) {
                 sigma_q = pow2_scale(fmaxf(ps[PS_RED + 2], ps[PS_RED + 3]));
                 iq = 1.f / sigma_q;
             }
         } else {
             iq = ps[PS_MISC + 5];
+            kappa = ps[PS_MISC + 6];
         }
         if (mt < 64) {  // the gate-dependent row scalars (rk, rq and the scales are the key head's)
-            const float rk = ps[PS_RK + mt];
+            const float rk = ps[PS_RK + mt], rkk = rk * (1.f / kappa);
             ps[PS_BBRK + mt] = expf(ps[PS_MISC + 0] - ps[PS_G + mt]) * rk;
-            ps[PS_TWF + mt] = ps[PS_BETA + mt] * ps[PS_E + mt] * rk;
-            ps[PS_DRK + mt] = ps[PS_D + mt] * rk;
+            ps[PS_TWF + mt] = ps[PS_BETA + mt] * ps[PS_E + mt] * rkk;
+            ps[PS_DRK + mt] = ps[PS_D + mt] * rkk;
             ps[PS_ER + mt] = SHARE ? ps[PS_E + mt] * ps[PS_RQ + mt] * iq : ps[PS_E + mt] * ps[PS_RQ + mt];  // Qt rows
             if (mt == 0 && vi == 0) {
                 ps[PS_MISC + 4] = 1.f / sigma;
+                ps[PS_MISC + 6] = kappa;
                 if constexpr (SHARE) ps[PS_MISC + 5] = iq;
             }
         }
@@ -1148,7 +1166,7 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         tc_fence_before();
         bar_sync(bar_id, 128);
         solve128(sA, sT, mt, bar_id);
-        {  // Tw' [t][s], Tb [m][s] (fp16) and Tb' = diag(d rk) T diag(beta) (fp16 hi + lo)
+        {  // Tw' [t][s], Tb [m][s] (fp16) and Tb' = diag(d rk / kappa) T diag(beta) (fp16 hi + lo)
             const int tt = mt >> 1, hh = mt & 1;
             const float drk = ps[PS_DRK + tt];
 #pragma unroll
@@ -1192,7 +1210,7 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         ab = !wait_bar(B + PB_M1, h & 1, budget);
         if (bar_any(bar_id, 128, ab)) { failed = true; break; }
         tc_fence_after();
-        {  // W^T row j -> WTd' = W^T diag(d rk) and WT (fp16) as TMEM A operands, in place
+        {  // W^T row j -> WTd' = W^T diag(d rk / kappa) and WT (fp16) as TMEM A operands, in place
             const int j = mt;
             uint32_t w0[32], w1[32];
             tmem_ld32_nw(P.tm + lane_off + PT_WT, w0);
@@ -1200,7 +1218,7 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
             tmem_wait_ld();
             (void)j;
             uint32_t a[32], b[32];
-            const float isg = ps[PS_MISC + 4];
+            const float isg = ps[PS_MISC + 4] * ps[PS_MISC + 6];  // kappa / sigma
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const float x0 = __uint_as_float(w0[2 * e]) * isg, x1 = __uint_as_float(w0[2 * e + 1]) * isg;
@@ -1215,9 +1233,9 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         }
         // the [B^T | E] image (bf16 hi + lo), staged in AT and then TT: image byte o -> stage address
         auto stage_be = [&](uint32_t o) { return o < BE_HEAD ? sm + PP_AT + o : sm + PP_TT + (o - BE_HEAD); };
-        {  // B^T row n (all 128 lanes), taken back by 1 / sigma: K-major [n][t]
+        {  // B^T row n (all 128 lanes), taken back by kappa / sigma: K-major [n][t]
             const int n = mt;
-            const float isg = ps[PS_MISC + 4];
+            const float isg = ps[PS_MISC + 4] * ps[PS_MISC + 6];  // kappa / sigma
             uint32_t bv[2][32];
             tmem_ld32_nw(P.tm + lane_off + PT_B, bv[0]);
             tmem_ld32_nw(P.tm + lane_off + PT_B + 32, bv[1]);
@@ -1299,7 +1317,7 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         if (bar_any(bar_id, 128, ab)) { failed = true; break; }
         {  // N row j -> fp16 (-N), MN-major [j][n] image in AT
             const int j = mt;
-            const float nsg = -ps[PS_MISC + 4];
+            const float nsg = -ps[PS_MISC + 4] * ps[PS_MISC + 6];  // -kappa / sigma
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t nv[32];

@@ -96,8 +96,9 @@ static_assert(CH_STAGE % 1024 == 0 && CH_V % 1024 == 0, "chain stages need 1 KiB
 // (image offsets below are byte offsets within a ring slot image; they are staged in dead buffers)
 constexpr uint32_t PP_RAW = 0;        // 32 KiB [kb 0..1][K rows 0..63 | Q rows 64..127][128 B] bf16; K rows -> fp16 (scaled)
 constexpr uint32_t PP_P = 32768;      //  8 KiB fp16 P [t][s]
-constexpr uint32_t PP_AT = 40960;     // 34 KiB: A fp32 [64][68] | T fp32 [64][68]; then the staged [B|E] head, N
+constexpr uint32_t PP_AT = 40960;     // 34 KiB: A fp32 [64][68] | T fp32 [64][68]; then Tw' lo; then the staged [B|E] head, N
 constexpr uint32_t PP_T = PP_AT + 17408;
+constexpr uint32_t PP_TWLO = PP_AT;   //  8 KiB fp16 Tw' lo [t][s], in A's place once the solve is done
 constexpr uint32_t PP_TT = 75776;     // 32 KiB: Tw' [t][s] | Tb [m][s] | Tb' hi [s][t] | Tb' lo (fp16); then [B|E] tail, Z
 constexpr uint32_t PP_SC = 108544;    //  4 KiB scalars
 constexpr uint32_t PP_BAR = 112640;   // mbarriers
@@ -107,7 +108,9 @@ constexpr uint32_t BE_HEAD = 34816;   // bytes of the [B|E] image staged in AT; 
 constexpr uint32_t Z_STAGE = 14336;   // Z image offset in TT (after the [B|E] tail)
 static_assert(2 * 24576 - BE_HEAD <= Z_STAGE && Z_STAGE + 16384 <= 32768, "staging overlaps");
 static_assert(32768 <= PP_TT - PP_AT, "N image does not fit in AT");
-static_assert(PP_BYTES % 1024 == 0 && PP_TT % 1024 == 0 && PP_P % 1024 == 0, "128B-swizzled tiles need 1 KiB alignment");
+static_assert(PP_BYTES % 1024 == 0 && PP_TT % 1024 == 0 && PP_P % 1024 == 0 && PP_TWLO % 1024 == 0,
+              "128B-swizzled tiles need 1 KiB alignment");
+static_assert(PP_TWLO + 8192 <= PP_T, "Tw' lo overlaps T");
 static_assert(PP_BAR + 256 <= PP_BYTES, "pipeline slice overflow");
 constexpr int LS = 68;                // row stride (floats) of A and T
 
@@ -881,9 +884,11 @@ __device__ void prep_control(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
         if (!wait_bar(B + PB_M1REQ, h & 1, budget)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks)  // (sigma / kappa) W^T = K'^T Tw'^T
-            mma_f16_ss(P.tm + PT_WT, desc_sw128(P.sb + PP_RAW + ks * 2048, 16384, 1024),
-                       desc_sw128(P.sb + PP_TT + ks * 32, 16, 1024), ID_WT, ks > 0);
+        for (int ks = 0; ks < 4; ++ks) {  // (sigma / kappa) W^T = K'^T Tw'^T (Tw' hi + lo)
+            const uint64_t ak = desc_sw128(P.sb + PP_RAW + ks * 2048, 16384, 1024);
+            mma_f16_ss(P.tm + PT_WT, ak, desc_sw128(P.sb + PP_TT + ks * 32, 16, 1024), ID_WT, ks > 0);
+            mma_f16_ss(P.tm + PT_WT, ak, desc_sw128(P.sb + PP_TWLO + ks * 32, 16, 1024), ID_WT, 1);
+        }
 #pragma unroll 1
         for (int ks = 0; ks < 4; ++ks) {  // (sigma / kappa) B^T = K'^T Tb' (hi + lo)
             const uint64_t ak = desc_sw128(P.sb + PP_RAW + ks * 2048, 16384, 1024);
@@ -1166,9 +1171,24 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
         tc_fence_before();
         bar_sync(bar_id, 128);
         solve128(sA, sT, mt, bar_id);
-        {  // Tw' [t][s], Tb [m][s] (fp16) and Tb' = diag(d rk / kappa) T diag(beta) (fp16 hi + lo)
+        // Tw' [t][s] and Tb' = diag(d rk / kappa) T diag(beta) as fp16 hi + lo, Tb [m][s] fp16. Tw' takes
+        // a lo part too: with nearly parallel keys W = Tw Kh cancels to a small fraction of its terms,
+        // and a single fp16 Tw' left the state's error at ~1e-3 of its norm.
+        {
             const int tt = mt >> 1, hh = mt & 1;
             const float drk = ps[PS_DRK + tt];
+            auto split16 = [](const float *x, uint4 &hi, uint4 &lo) {  // x = hi + lo + O(2^-22 |x|)
+                hi = pack8_f16(x, 1.f);
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&hi);
+                float r[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    r[2 * e] = x[2 * e] - f.x;
+                    r[2 * e + 1] = x[2 * e + 1] - f.y;
+                }
+                lo = pack8_f16(r, 1.f);
+            };
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
                 float tw[8], tb[8], tp[8];
@@ -1186,21 +1206,14 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
                     }
                 }
                 const int c = 4 * hh + c8;
-                *reinterpret_cast<uint4 *>(sm + PP_TT + swz(tt, c)) = pack8_f16(tw, 1.f);
+                uint4 hi, lo;
+                split16(tw, hi, lo);
+                *reinterpret_cast<uint4 *>(sm + PP_TT + swz(tt, c)) = hi;
+                *reinterpret_cast<uint4 *>(sm + PP_TWLO + swz(tt, c)) = lo;
                 *reinterpret_cast<uint4 *>(sm + PP_TT + 8192 + swz(tt, c)) = pack8_f16(tb, 1.f);
-                float lo[8];
-                const uint4 hi = pack8_f16(tp, 1.f);
-                {
-                    const __half2 *hv2 = reinterpret_cast<const __half2 *>(&hi);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(hv2[e]);
-                        lo[2 * e] = tp[2 * e] - f.x;
-                        lo[2 * e + 1] = tp[2 * e + 1] - f.y;
-                    }
-                }
+                split16(tp, hi, lo);
                 *reinterpret_cast<uint4 *>(sm + PP_TT + 16384 + swz(tt, c)) = hi;
-                *reinterpret_cast<uint4 *>(sm + PP_TT + 24576 + swz(tt, c)) = pack8_f16(lo, 1.f);
+                *reinterpret_cast<uint4 *>(sm + PP_TT + 24576 + swz(tt, c)) = lo;
             }
         }
         fence_async_smem();

@@ -7,6 +7,11 @@ from its unit-scale value (the layer normalises q and k, so the outputs barely c
 and initial states scaled by 1e4 or 1e-4 put the state beyond fp16's range or into its
 subnormals, where only the row scales keep it exact to fp16 precision. The parity bars are
 relative (output max-abs / RMS, state relative Frobenius), so they hold at every scale.
+
+The last cases draw nearly identical keys with beta close to 1, where A = beta e^{G_t-G_s} kh_t.kh_s
+is close to a strictly lower matrix of ones, the triangular solve (I + A)^-1 does the most work and
+W = T diag(beta e) Kh cancels to a small fraction of its terms. They run on the ring kernel (the
+default tensor-core path), which carries T diag(beta e) as fp16 hi + lo for this reason.
 """
 import dataclasses
 
@@ -70,3 +75,24 @@ def test_cluster_kernel(qk, vs, monkeypatch):
     b = inputs.make_batch(Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", chunk=64, seed=73, init_state=True,
                           slow_gate=True, lengths=[65, 300])
     run_and_check(scaled(b, qk, vs))
+
+
+def correlated_keys(batch, spread=0.05, beta_logit=4.0):
+    """Every key of a key head is that head's first key plus spread x N(0, 1) noise; beta logits
+    raised by beta_logit (beta near 1). Seeded from the batch's own seed."""
+    gen = torch.Generator().manual_seed(int(batch.meta["seed"]) + 500)
+    k = batch.k.float()
+    k = k[:1].expand_as(k) + spread * torch.randn(k.shape, generator=gen)
+    return dataclasses.replace(batch, k=k.to(batch.k.dtype), b=(batch.b.float() + beta_logit).to(batch.b.dtype))
+
+
+def test_correlated_keys_ring_kernel():
+    b = inputs.make_batch(B=1, T=700, Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", chunk=64, seed=74,
+                          init_state=True, slow_gate=True)
+    run_and_check(correlated_keys(b))
+
+
+def test_correlated_keys_ring_kernel_key_sharing():
+    b = inputs.make_batch(Hk=20, Hv=40, dk=128, dv=128, dtype="bf16", chunk=64, seed=75, init_state=True,
+                          lengths=[190, 64, 333])
+    run_and_check(correlated_keys(b), key_heads=[0, 11])

@@ -101,6 +101,13 @@ typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
  * token scan instead: every state row is read once, takes the T updates in
  * order in registers, and is written once, so T steps cost one pass over the
  * state. The result is the same function (only the rounding order differs).
+ * Accuracy: the tensor-core kernels multiply fp16 or bf16 operands into fp32 accumulators,
+ * with power-of-two scales chosen at run time (so the fp16 operands stay in range whatever the
+ * scale of q, k, v and the state) and operands that carry v into the state, or that cancel,
+ * split into hi + lo pairs. Against an fp64 token scan the final states stay within 1e-3
+ * (relative Frobenius) and the outputs within 2e-2 x RMS (max-abs) plus their one rounding to
+ * the output dtype; measured on random inputs, slow and fast gates, q and k scaled by 1e-3 to
+ * 300, v and states by 1e-4 to 1e4, and nearly parallel keys with beta near 1.
  * The tensor-core path needs device scratch (see gdn_prefill_workspace_size); gdn_prefill
  * keeps one workspace per device for it, allocated by the first call that needs it and grown
  * (after the work using the old one has finished) when a call needs more. Calls on different

@@ -101,7 +101,7 @@ typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
  * token scan instead: every state row is read once, takes the T updates in
  * order in registers, and is written once, so T steps cost one pass over the
  * state. The result is the same function (only the rounding order differs).
- * Accuracy: the tensor-core kernels multiply fp16 or bf16 operands into fp32 accumulators,
+ * Accuracy: the tensor-core kernel multiplies fp16 or bf16 operands into fp32 accumulators,
  * with power-of-two scales chosen at run time (so the fp16 operands stay in range whatever the
  * scale of q, k, v and the state) and operands that carry v into the state, or that cancel,
  * split into hi + lo pairs. Against an fp64 token scan the final states stay within 1e-3

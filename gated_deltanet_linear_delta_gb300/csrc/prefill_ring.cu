@@ -35,10 +35,14 @@
 // is consumed. Units are handed out in step order, so every wait is for a unit handed out
 // earlier, and a prep CTA publishes what it has written before it waits for a slot: no cycle.
 //
-// Numerics (per-operand rounding validated against the fp64 token scan): N, Z, Kh, W in fp16;
-// S in fp16 with an exact power-of-two scale per row for the MMAs, fp32 everywhere else; B and
-// E (which carry v into the state and the outputs) as bf16 hi + lo pairs against the raw bf16
-// V tile; every accumulator fp32.
+// Numerics (per-operand rounding validated against the fp64 token scan): N, Z, W and P in fp16;
+// K in fp16 as sigma K (exact: a power-of-two sigma from the tile's largest magnitude); S in fp16
+// with an exact power-of-two scale per row for the MMAs, fp32 everywhere else; B and E (which
+// carry v into the state and the outputs) as bf16 hi + lo pairs against the raw bf16 V tile;
+// T diag(beta e rk) and diag(d rk) T diag(beta) as fp16 hi + lo (W and B cancel to a small
+// fraction of their terms when keys are nearly parallel), with rk divided by a power of two
+// kappa >= max rk so that keys of any norm keep them out of fp16's subnormals; every scale is
+// taken back in fp32; every accumulator fp32.
 //
 // Rows t >= L of a partial block get zero kh, qh, beta and d, so they contribute nothing; their
 // outputs are not stored. Every wait is bounded; a wait that runs out sets the device status

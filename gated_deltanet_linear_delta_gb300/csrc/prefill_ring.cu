@@ -196,6 +196,9 @@ __device__ __forceinline__ int row_exp(float m) {
     return max(-100, min(100, e));
 }
 
+// four consecutive per-row scalars from the 16-byte aligned scalar area (index a multiple of 4)
+__device__ __forceinline__ float4 ps4(const float *ps, int i) { return *reinterpret_cast<const float4 *>(ps + i); }
+
 // the power of two 2^e just above m (m < 2^e), clamped; 1 for m <= 0 or non-finite
 __device__ __forceinline__ float pow2_above(float m) {
     if (!(m > 0.f) || !isfinite(m)) return 1.f;
@@ -1150,12 +1153,27 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
             if (ps[PS_MISC + 2] != 0.f) {  // e^{G_t-G_s} = a_t b_s (uniform over the CTA)
                 const float at = nt * ps[PS_AA + row];
 #pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(gv[e >> 5][e & 31]) * at * ps[PS_BBRK + e];
+                for (int e4 = 0; e4 < 16; ++e4) {
+                    const float4 bb = ps4(ps, PS_BBRK + 4 * e4);
+                    const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int e = 4 * e4 + u;
+                        x[e] = __uint_as_float(gv[e >> 5][e & 31]) * at * bv[u];
+                    }
+                }
             } else {  // a gate range too wide to factor: one exponential per element
                 const float Gt = ps[PS_G + row];
 #pragma unroll
-                for (int e = 0; e < 64; ++e)
-                    x[e] = __uint_as_float(gv[e >> 5][e & 31]) * nt * ps[PS_RK + e] * __expf(Gt - ps[PS_G + e]);
+                for (int e4 = 0; e4 < 16; ++e4) {
+                    const float4 r4 = ps4(ps, PS_RK + 4 * e4), g4 = ps4(ps, PS_G + 4 * e4);
+                    const float rv[4] = {r4.x, r4.y, r4.z, r4.w}, gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int e = 4 * e4 + u;
+                        x[e] = __uint_as_float(gv[e >> 5][e & 31]) * nt * rv[u] * __expf(Gt - gg[u]);
+                    }
+                }
             }
             if (isq) {
 #pragma unroll
@@ -1201,11 +1219,12 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
                     const int s0 = 32 * hh + 8 * c8 + 4 * c4;
                     const float4 t4 = *reinterpret_cast<const float4 *>(sT + tt * LS + s0);
                     const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+                    const float4 b4 = ps4(ps, PS_BETA + s0), w4 = ps4(ps, PS_TWF + s0);
+                    const float bev[4] = {b4.x, b4.y, b4.z, b4.w}, twv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float be = ps[PS_BETA + s0 + e];
-                        tb[4 * c4 + e] = tv[e] * be;
-                        tw[4 * c4 + e] = tv[e] * ps[PS_TWF + s0 + e];
+                        tb[4 * c4 + e] = tv[e] * bev[e];
+                        tw[4 * c4 + e] = tv[e] * twv[e];
                         tp[4 * c4 + e] = tb[4 * c4 + e] * drk;
                     }
                 }
@@ -1237,13 +1256,19 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
             uint32_t a[32], b[32];
             const float isg = ps[PS_MISC + 4] * ps[PS_MISC + 6];  // kappa / sigma
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float x0 = __uint_as_float(w0[2 * e]) * isg, x1 = __uint_as_float(w0[2 * e + 1]) * isg;
-                const float y0 = __uint_as_float(w1[2 * e]) * isg, y1 = __uint_as_float(w1[2 * e + 1]) * isg;
-                a[e] = h2_bits(x0 * ps[PS_DRK + 2 * e], x1 * ps[PS_DRK + 2 * e + 1]);
-                a[16 + e] = h2_bits(y0 * ps[PS_DRK + 32 + 2 * e], y1 * ps[PS_DRK + 33 + 2 * e]);
-                b[e] = h2_bits(x0, x1);
-                b[16 + e] = h2_bits(y0, y1);
+            for (int e2 = 0; e2 < 8; ++e2) {
+                const float4 d0 = ps4(ps, PS_DRK + 4 * e2), d1 = ps4(ps, PS_DRK + 32 + 4 * e2);
+                const float dv0[4] = {d0.x, d0.y, d0.z, d0.w}, dv1[4] = {d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int e = 2 * e2 + u;
+                    const float x0 = __uint_as_float(w0[2 * e]) * isg, x1 = __uint_as_float(w0[2 * e + 1]) * isg;
+                    const float y0 = __uint_as_float(w1[2 * e]) * isg, y1 = __uint_as_float(w1[2 * e + 1]) * isg;
+                    a[e] = h2_bits(x0 * dv0[2 * u], x1 * dv0[2 * u + 1]);
+                    a[16 + e] = h2_bits(y0 * dv1[2 * u], y1 * dv1[2 * u + 1]);
+                    b[e] = h2_bits(x0, x1);
+                    b[16 + e] = h2_bits(y0, y1);
+                }
             }
             tmem_st32(P.tm + lane_off + PT_WT, a);
             tmem_st32(P.tm + lane_off + PT_WT + 32, b);
@@ -1312,6 +1337,8 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     float x[8];
+                    const float4 r0 = ps4(ps, PS_ER + 32 * q + 8 * cc), r1 = ps4(ps, PS_ER + 32 * q + 8 * cc + 4);
+                    const float er[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int t = 32 * q + 8 * cc + e, row = 64 + t;
@@ -1321,7 +1348,7 @@ __device__ void prep_math(const RingParams &p, const Pipe &P, int mt, int bar_id
                             qf = __half2float(*reinterpret_cast<const __half *>(qa));
                         else
                             qf = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa));
-                        x[e] = ps[PS_ER + t] * qf - __uint_as_float(wv[8 * cc + e]);
+                        x[e] = er[e] * qf - __uint_as_float(wv[8 * cc + e]);
                     }
                     *reinterpret_cast<uint4 *>(sm + PP_TT + Z_STAGE + swz(j, 4 * q + cc)) = pack8_f16(x, 1.f);
                 }

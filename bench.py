@@ -46,7 +46,7 @@ PREFILL_FLOPS_PER_TOKEN = HV * (5 * 2 * CHUNK * DK + 3 * 2 * DK * DV)  # chunk G
 DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + IO_BYTES_PER_TOKEN
 # DRAM bytes per launch from the committed ncu captures (profiles/); None once a kernel
 # has changed since its capture.
-TRAFFIC = {"prefill": None, "decode": 480.2e6, "scan": 488.7e6}
+TRAFFIC = {"prefill": 129.6e6, "decode": 480.2e6, "scan": 488.7e6}
 # nominal GB300 figures, reported beside the measured denominators
 NOMINAL_HBM_GBS, NOMINAL_BF16_TFLOPS = 7900.0, 2250.0
 
